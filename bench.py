@@ -1,0 +1,418 @@
+#!/usr/bin/env python3
+"""Benchmark of one pass of the shared-prefix classifier path on GB300.
+
+A step is one whole pass over one batch of synthetic input: host planning
+(token trie, staged rounds, KV pages, launch lists) and descriptor upload,
+every round's prefix and branch attention (KV append into the paged pool,
+cascade attention, split merges), the fused LM-head readout and the label
+softmax.  The default workload is the yes/no configuration: Hq 32 / Hkv 4 /
+d 128, a 2000-token shared prefix with 5 branches of 48 tokens, H 2048,
+V 151936, two labels per branch.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                       [--config NAME]
+Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "branch-prefill tokens/s & label decisions/s at 1 GB300; % of roofline"
+DEFAULT_CONFIG = "yesno"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="libsp", choices=["libsp", "reference"])
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# --------------------------------------------------------------------------
+# clocks sampled during the timed region
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def kernel_traffic(kernel_file: str, config: str):
+    """dram bytes per launch from the committed ncu summary, if the kernel
+    source is unchanged since it was captured; else None."""
+    src = os.path.join(ROOT, "prefill_only_shared_gb300", "csrc", kernel_file)
+    summ = os.path.join(ROOT, "profiles", f"traffic_{os.path.splitext(kernel_file)[0]}_{config}.json")
+    if not (os.path.exists(src) and os.path.exists(summ)):
+        return None
+    d = json.load(open(summ))
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    if d.get("source_sha256") != sha:
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# --------------------------------------------------------------------------
+def attention_flops(plan_segments, wl):
+    """Algorithmic attention FLOPs of one pass: 4 * d * Hq per (query, visible
+    key) pair (2 for q.k, 2 for p.v), over every computed row."""
+    import numpy as np
+    sh = wl.shape
+    seg = plan_segments
+    n = len(seg["len"])
+    ctx_before = np.zeros(n, dtype=np.int64)
+    for s in range(n):
+        p = seg["parent"][s]
+        ctx_before[s] = 0 if p < 0 else ctx_before[p] + seg["len"][p]
+    prefix, branch = 0, 0
+    for s in range(n):
+        L = int(seg["len"][s])
+        pairs = L * int(ctx_before[s]) + L * (L + 1) // 2
+        if seg["shared"][s]:
+            prefix += pairs
+        else:
+            branch += pairs
+    f = 4 * sh.head_dim * sh.n_q_heads
+    return prefix * f, branch * f
+
+
+def run_libsp(args, ws, rank, local):
+    import numpy as np
+    import torch
+    from prefill_only_shared_gb300 import build as B
+    B.ensure_built()
+    from prefill_only_shared_gb300 import sp
+    from prefill_only_shared_gb300.pipeline import SharedPrefixClassifier
+    from prefill_only_shared_gb300.workloads import make_workload
+
+    torch.cuda.set_device(local)
+    dev = torch.device(f"cuda:{local}")
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    wl = make_workload(args.config, seed=0)
+    sh = wl.shape
+    clf = SharedPrefixClassifier(sh.n_q_heads, sh.n_kv_heads, sh.head_dim, sh.hidden, sh.vocab,
+                                 device=dev)
+    q, k, v = wl.q.to(dev), wl.k.to(dev), wl.v.to(dev)
+    h, W = wl.h.to(dev), wl.W.to(dev)
+    off = torch.from_numpy(wl.label_off).to(dev)
+    ids = torch.from_numpy(wl.label_ids).to(dev)
+    n_labels = int(wl.label_ids.shape[0])
+    N = wl.n_branches
+    stream = torch.cuda.current_stream(dev)
+
+    # events around the readout call of every timed step (dominant kernel)
+    def step(ev=None):
+        plan = clf.plan(wl.req_of_branch, wl.tok_offsets, wl.tokens)
+        if ev is not None:
+            ev[0].record(stream)
+        clf.attention(plan, q, k, v, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        logprobs, lse, probs, am = clf.readout(h, W, off, ids, n_labels, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        return plan
+
+    plan = step()
+    torch.cuda.synchronize()
+    sp.sp_check_device_error()
+    stats = plan.stats()
+    segs = plan.segments()
+    launches_per_step = clf.last_launches
+    branch_tokens = int(sum(segs["len"][i] for i in range(len(segs["len"])) if not segs["shared"][i]))
+    branch_tokens += int(plan.branches()["recompute"].sum())
+    f_prefix, f_branch = attention_flops(segs, wl)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # phase events inside the timed region
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_stop = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_stop.record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    total_ms = t_start.elapsed_time(t_stop)
+    attn_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    lm_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    if ws > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    sp.sp_check_device_error()
+
+    # ---- end-to-end through the public call, host buffers --------------------
+    pin = lambda x: x.pin_memory()
+    hq, hk, hv, hh = pin(wl.q), pin(wl.k), pin(wl.v), pin(wl.h)
+    hoff = pin(torch.from_numpy(wl.label_off))
+    hids = pin(torch.from_numpy(wl.label_ids))
+    out_probs = torch.empty(n_labels, dtype=torch.float32).pin_memory()
+    out_am = torch.empty(N, dtype=torch.int32).pin_memory()
+    dq, dk, dv, dh = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(h)
+    doff, dids = torch.empty_like(off), torch.empty_like(ids)
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hh, hoff, hids))
+    h2d += wl.tokens.nbytes + wl.tok_offsets.nbytes + wl.req_of_branch.nbytes  # read by the planner
+    d2h = out_probs.numel() * 4 + out_am.numel() * 4
+
+    def e2e_step():
+        for d_, s_ in ((dq, hq), (dk, hk), (dv, hv), (dh, hh), (doff, hoff), (dids, hids)):
+            d_.copy_(s_, non_blocking=True)
+        res = clf.run(wl.req_of_branch, wl.tok_offsets, wl.tokens, dq, dk, dv, dh, W, doff, dids,
+                      stream)
+        out_probs.copy_(res.probs, non_blocking=True)
+        out_am.copy_(res.argmax, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        torch.distributed.barrier()
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    if ws > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    sp.sp_check_device_error()
+
+    ms = total_ms / args.steps
+    value = branch_tokens * ws / (ms / 1e3)
+    peaks, peak_kind = load_peaks()
+    lm_avg = statistics.mean(lm_ms)
+    attn_avg = statistics.mean(attn_ms)
+    lm_bytes = sh.vocab * sh.hidden * 2 + N * sh.hidden * 2 + n_labels * 8 + N * 4
+    achieved = lm_bytes / (lm_avg / 1e3) / 1e9
+    attn_flops = f_prefix + f_branch
+    result = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "branch tokens/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded, BASELINE shapes; random-init LM head)",
+        "config": {
+            "workload": f"{args.config}: Hq {sh.n_q_heads}/Hkv {sh.n_kv_heads}/d {sh.head_dim}, "
+                        f"{N} branches, {stats['logical_tokens']} logical tokens, "
+                        f"{stats['computed_tokens']} computed, H {sh.hidden}, V {sh.vocab}",
+            "branches": N,
+            "branch_tokens_per_step": branch_tokens,
+            "logical_tokens_per_step": stats["logical_tokens"],
+            "rounds": stats["n_rounds"],
+            "l2": "inputs larger than L2 (the 622 MB LM head is streamed every step)",
+            "parallelism": f"replicas x{ws} (independent workloads per GPU)",
+        },
+        "decisions_per_s": round(N * ws / (ms / 1e3), 1),
+        "logical_tokens_per_s": round(stats["logical_tokens"] * ws / (ms / 1e3), 1),
+        "phase_ms": {"attention": round(attn_avg, 5), "readout": round(lm_avg, 5),
+                     "plan_and_launch_overhead": round(ms - attn_avg - lm_avg, 5)},
+        "roofline": {
+            "kernel": "lmhead_kernel (+ its finalize launch)",
+            "bound": "hbm",
+            "achieved": round(achieved, 1),
+            "peak": peaks["hbm_gbs"],
+            "unit": "GB/s",
+            "frac": round(achieved / peaks["hbm_gbs"], 4),
+            "traffic": kernel_traffic("lmhead.cu", args.config),
+            "peak_source": f"{peak_kind} hbm_gbs",
+            "algorithmic_bytes_per_launch": lm_bytes,
+        },
+        "attention_roofline": {
+            "bound": "tensor",
+            "achieved": round(attn_flops / (attn_avg / 1e3) / 1e12, 2),
+            "peak": peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]),
+            "unit": "TFLOP/s",
+            "frac": round(attn_flops / (attn_avg / 1e3) / 1e12 /
+                          peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]), 4),
+            "algorithmic_flops_per_step": attn_flops,
+            "note": "all attention calls of a step incl. KV append and merges",
+        },
+        "e2e": {"value": round(branch_tokens * ws / (e2e_ms / 1e3), 1), "unit": "branch tokens/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "ms_per_step": round(e2e_ms, 5)},
+        "gpu_launches": int(launches_per_step * args.steps),
+        "clocks": clocks,
+    }
+    if rank == 0:
+        result["cpu_baseline"] = cpu_baseline(wl, args.config)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return result if rank == 0 else None
+
+
+# --------------------------------------------------------------------------
+def oracle_sample(wl, n_branches: int):
+    """The oracle on a bounded sample: n_branches branches recomputed unshared
+    (full sequence attention), their full-vocabulary readout and softmax."""
+    import numpy as np
+    from oracle import attention as OA
+    from oracle import label_softmax as OL
+    from oracle import readout as OR
+    from oracle import staging as OS
+    plan = OS.build_plan(wl.req_of_branch, wl.tok_offsets, wl.tokens)
+    br = list(range(min(n_branches, wl.n_branches)))
+    OA.reference_attention(plan, wl.q, wl.k, wl.v, branches=br)
+    lp, _ = OR.label_logprobs(wl.h, wl.W, wl.label_off, wl.label_ids, branches=br)
+    off = np.concatenate([[0], np.cumsum([wl.label_off[b + 1] - wl.label_off[b] for b in br])])
+    OL.label_softmax(lp, off)
+    suffix = sum(plan.segments[plan.paths[b][-1]].length for b in br)
+    return suffix, len(br)
+
+
+def cpu_baseline(wl, config, n_branches=1):
+    import torch
+    torch.set_num_threads(os.cpu_count() or 1)
+    t = time.perf_counter()
+    toks, nb = oracle_sample(wl, n_branches)
+    dt = time.perf_counter() - t
+    return {"value": round(toks / dt, 3), "unit": "branch tokens/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"{config}: {nb} branch(es) recomputed unshared in float64 (full-sequence "
+                      f"attention, full-vocabulary readout, softmax); {dt:.1f} s"}
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return None
+    from prefill_only_shared_gb300.workloads import make_workload
+    import torch
+    torch.set_num_threads(os.cpu_count() or 1)
+    wl = make_workload(args.config, seed=0)
+    for _ in range(args.warmup):
+        oracle_sample(wl, 1)
+    t = time.perf_counter()
+    toks = 0
+    for _ in range(args.steps):
+        tk, _ = oracle_sample(wl, 1)
+        toks += tk
+    dt = time.perf_counter() - t
+    value = toks / dt
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 3), "unit": "branch tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded, BASELINE shapes)",
+        "config": {"workload": args.config, "sample": "1 branch per step"},
+        "cpu_baseline": {"value": round(value, 3), "unit": "branch tokens/s",
+                         "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": f"{args.config}: 1 branch per step recomputed unshared in "
+                                   "float64 (attention, full-vocabulary readout, softmax)"},
+        "e2e": {"value": round(value, 3), "unit": "branch tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        res = run_reference(args, ws, rank)
+    else:
+        res = run_libsp(args, ws, rank, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

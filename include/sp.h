@@ -1,0 +1,246 @@
+/*
+ * libsp -- shared-prefix, prefill-only label readout on GB300 (sm_103a).
+ *
+ * The method (openjev-sglang article on jdon.com, sections on the request
+ * flow and on what prefill-only means; LLM2Jev "shared prefix" page): one
+ * shared state prefix is prefilled once, every question branch (prefix +
+ * question suffix) is prefilled against the cached prefix, and each branch's
+ * last position is read out as log-probabilities of a few single-token labels,
+ * renormalised with a stable softmax.  There is no decode.
+ *
+ * This header is the whole boundary.  All entry points are plain C; every
+ * pointer is either HOST memory or DEVICE memory as stated per argument; no
+ * entry point allocates device memory (pools, outputs, descriptors and
+ * workspaces are all owned by the caller).  Device work is enqueued on the
+ * caller's stream (`stream` is a cudaStream_t; NULL = legacy default stream)
+ * and is asynchronous: a returned SP_OK means the launch was accepted.
+ *
+ * Errors: argument and limit errors are detected on the host BEFORE anything
+ * is launched (the article's rule that every rejection happens before
+ * inference).  Errors that only the device can see (an out-of-range label id,
+ * a label count outside [2, 64], a bounded wait that gave up) set a sticky
+ * device error word, read and cleared by sp_check_device_error().
+ *
+ * Threading: a plan is immutable after sp_plan_build and may be read by
+ * several threads; calls that share a KV pool, output or workspace must be
+ * ordered by the caller (one stream, or events).
+ */
+#ifndef SP_H_
+#define SP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum sp_status {
+  SP_OK = 0,
+  SP_ERR_ARG = 1,            /* bad pointer, shape, count or id (host-checked)    */
+  SP_ERR_LIMIT = 2,          /* request limits: >32768 tokens per branch,
+                                >262144 logical tokens per request              */
+  SP_ERR_POOL_FULL = 3,      /* the plan needs more KV pages than max_pages      */
+  SP_ERR_CUDA = 4,           /* a CUDA runtime call or launch failed             */
+  SP_ERR_DEVICE_TIMEOUT = 5, /* a kernel's bounded wait gave up (device word)    */
+  SP_ERR_DEVICE_BOUNDS = 6,  /* a device-side bounds check failed (device word)  */
+  SP_ERR_WORKSPACE = 7       /* workspace / descriptor buffer too small          */
+} sp_status;
+
+/* Model shape of the single attention layer and the LM head.
+ * n_q_heads % n_kv_heads == 0 and the group n_q_heads / n_kv_heads divides
+ * 128 (grouped-query attention, contiguous groups: query head h reads KV head
+ * h / group); head_dim is 64 or 128; page_size must be 16 tokens; hidden is a
+ * multiple of 8 (16-byte rows); vocab >= 2. */
+typedef struct sp_shape {
+  int32_t n_q_heads;
+  int32_t n_kv_heads;
+  int32_t head_dim;
+  int32_t page_size;
+  int32_t hidden;
+  int32_t vocab;
+} sp_shape;
+
+/* Opaque host-side plan (token trie, segments, rounds, pages, launch lists). */
+typedef struct sp_plan sp_plan;
+
+/* Token accounting of a plan.  logical_tokens counts every branch's full
+ * input, as usage is reported on both pages (cache hits do not reduce it);
+ * computed_tokens counts each trie segment once plus one row per branch whose
+ * final position is recomputed; reused = logical - computed. */
+typedef struct sp_plan_stats {
+  int64_t n_requests;
+  int64_t n_branches;
+  int64_t n_segments;
+  int64_t n_shared_segments;
+  int64_t n_rounds;
+  int64_t logical_tokens;
+  int64_t computed_tokens;
+  int64_t reused_tokens;
+  int64_t node_tokens;       /* rows of the node-token arrays q/k/v/out/lse      */
+  int64_t pages_used;
+  int64_t desc_bytes;        /* size of the device descriptor (sp_plan_upload)    */
+  int64_t attn_workspace_bytes; /* workspace needed by the attention calls      */
+} sp_plan_stats;
+
+/* Build a plan from the branches' full token sequences.
+ *
+ * Source: LLM2Jev "shared prefix" page (sharing is decided on the tokenised
+ * prefix; staged submission for a cold request) and the openjev-sglang
+ * article (radix cache; request limits).
+ *
+ *   n_branches      number of branches (candidates), >= 1
+ *   req_of_branch   HOST int32[n_branches]; request id of each branch; branches
+ *                   of different requests never share a segment
+ *   tok_offsets     HOST int64[n_branches+1]; CSR offsets into tokens
+ *   tokens          HOST int32[tok_offsets[n_branches]]; every branch >= 1 token
+ *   max_pages       capacity of the caller's KV pool in pages
+ *   n_sms           SM count used to size split-KV work (<= 0: 152)
+ *   out             receives the plan; free with sp_plan_free
+ *
+ * Segments (trie nodes) are laid out in "node-token" order: requests in
+ * increasing request id, each request's
+ * segments in depth-first pre-order with children ordered by the smallest
+ * branch index passing through them.  q/k/v/out/lse rows use that order
+ * (sp_plan_segments gives each segment's first row).  Every segment starts on
+ * a fresh KV page; pages are numbered 0..pages_used-1 in segment order.
+ *
+ * Rounds: per request, scan unscored branches in order; a branch joins the
+ * round unless one of its uncached shared segments was already claimed by an
+ * earlier branch of the same round; joining branches claim their uncached
+ * shared segments.  Round r of the plan is the union over requests.
+ *
+ * Errors: SP_ERR_ARG (null pointer, bad shape, empty branch, negative request
+ * id), SP_ERR_LIMIT (branch > 32768 tokens or request > 262144 logical
+ * tokens), SP_ERR_POOL_FULL (pages needed > max_pages). */
+sp_status sp_plan_build(const sp_shape* shape, int32_t n_branches, const int32_t* req_of_branch,
+                        const int64_t* tok_offsets, const int32_t* tokens, int32_t max_pages,
+                        int32_t n_sms, sp_plan** out);
+
+void sp_plan_free(sp_plan* plan);
+
+sp_status sp_plan_get_stats(const sp_plan* plan, sp_plan_stats* out);
+
+/* Round lists: round r holds round_branches[round_offsets[r] .. round_offsets[r+1]),
+ * in increasing branch order.  Views into the plan, valid until sp_plan_free. */
+sp_status sp_plan_rounds(const sp_plan* plan, int32_t* n_rounds, const int32_t** round_offsets,
+                         const int32_t** round_branches);
+
+/* Segment table (views, length n_segments): request, parent (-1 for a request
+ * root), first node-token row, length, round in which it is computed, whether
+ * it is shared by >= 2 branches, first KV page. */
+sp_status sp_plan_segments(const sp_plan* plan, int32_t* n_segments, const int32_t** seg_req,
+                           const int32_t** seg_parent, const int64_t** seg_node_start,
+                           const int32_t** seg_len, const int32_t** seg_round,
+                           const int32_t** seg_shared, const int32_t** seg_first_page);
+
+/* Per-branch views (length n_branches): segment holding the last token, the
+ * node-token row of the last token (the readout position), the branch's
+ * round, and 1 when the last row is recomputed because it was cached before
+ * the branch's round (the final scoring position is always computed). */
+sp_status sp_plan_branches(const sp_plan* plan, const int32_t** branch_last_seg,
+                           const int64_t** branch_last_row, const int32_t** branch_round,
+                           const int32_t** branch_recompute);
+
+/* Host view of the device descriptor image (what sp_plan_upload copies):
+ * a header of byte offsets and counts followed by the segment table, page
+ * table, ancestor chains, append list, tile list and merge list. */
+sp_status sp_plan_descriptor(const sp_plan* plan, const void** data, size_t* bytes);
+
+/* Launch lists of one call (kind 0 = sp_prefix_attn, 1 = sp_branch_attn) of
+ * `round`: info[0..6] = append offset, appends, tile offset, tiles, merge
+ * offset, merges (entries of the descriptor lists), partial slots used. */
+sp_status sp_plan_call_info(const sp_plan* plan, int32_t round, int32_t kind, int64_t info[7]);
+
+/* Copy the plan's device descriptor (stats.desc_bytes bytes) into the
+ * caller's DEVICE buffer dev_desc (>= 256-byte aligned) on `stream`.  The host
+ * source lives in the plan: keep the plan alive until the copy completes. */
+sp_status sp_plan_upload(const sp_plan* plan, void* dev_desc, size_t bytes, void* stream);
+
+/* Shared-prefix attention for the segments first computed in `round`.
+ *
+ * sp_prefix_attn handles the shared segments claimed in the round (the
+ * article's shared-prefix prefill, computed once); sp_branch_attn handles the
+ * branches' own suffixes (the branch prefill against the cached prefix) and
+ * recomputed final rows.  Both first append the segments' K/V into the pool,
+ * then compute causal softmax attention of every new row over its ancestor
+ * segments (read from the pool) and its own segment (causal), scale
+ * 1/sqrt(head_dim), and merge the levels with a log-sum-exp combine.
+ *
+ *   dev_desc  DEVICE, the uploaded descriptor of this plan
+ *   round     0 <= round < n_rounds; calls must run in round order, and the
+ *             prefix call of a round before its branch call
+ *   q         DEVICE bf16 [node_tokens, n_q_heads, head_dim]
+ *   k, v      DEVICE bf16 [node_tokens, n_kv_heads, head_dim]
+ *   kv_pool   DEVICE bf16 [max_pages, 2 (K,V), n_kv_heads, page_size, head_dim]
+ *   out       DEVICE bf16 [node_tokens, n_q_heads, head_dim]; rows of this
+ *             call's segments are written (round to nearest even)
+ *   lse       DEVICE fp32 [node_tokens, n_q_heads]; natural-log sum of exp of
+ *             the scaled scores of each written row
+ *   workspace DEVICE, >= stats.attn_workspace_bytes, 256-byte aligned
+ * All device pointers 16-byte aligned. */
+sp_status sp_prefix_attn(const sp_plan* plan, const void* dev_desc, int32_t round, const void* q,
+                         const void* k, const void* v, void* kv_pool, void* out, float* lse,
+                         void* workspace, size_t ws_bytes, void* stream);
+
+sp_status sp_branch_attn(const sp_plan* plan, const void* dev_desc, int32_t round, const void* q,
+                         const void* k, const void* v, void* kv_pool, void* out, float* lse,
+                         void* workspace, size_t ws_bytes, void* stream);
+
+/* Workspace bytes for sp_label_logprobs with n_branches rows. */
+size_t sp_label_workspace_bytes(int32_t n_branches, int32_t vocab, int32_t n_sms);
+
+/* Final-position LM-head readout (openjev-sglang article, prefill-only
+ * section: log-probabilities of the requested label ids at the last position):
+ *
+ *   logits[n, v] = sum_k h[n, k] W[v, k];  lse[n] = ln sum_v exp(logits[n, v])
+ *   logprobs[j]  = logits[n(j), label_ids[j]] - lse[n(j)]
+ *
+ * computed in one streaming pass over W with tensor cores; logits are never
+ * written to memory.
+ *
+ *   h          DEVICE bf16 [N, H] (row-major), final hidden states
+ *   W          DEVICE bf16 [V, H] (row-major), LM head
+ *   N          1 <= N <= 4096 branches;  H: multiple of 8;  V >= 2
+ *   label_off  DEVICE int32 [N+1] CSR offsets (label_off[0] = 0)
+ *   label_ids  DEVICE int32 [n_labels] with 0 <= id < V
+ *   n_labels   label_off[N] (host copy of the total)
+ *   logprobs   DEVICE fp32 [n_labels];  lse: DEVICE fp32 [N]
+ *   workspace  DEVICE, >= sp_label_workspace_bytes(N, V, n_sms), 16-byte aligned
+ * Device-side checks: an id outside [0, V) yields NaN and SP_ERR_DEVICE_BOUNDS. */
+sp_status sp_label_logprobs(const void* h, const void* W, int32_t N, int32_t H, int32_t V,
+                            const int32_t* label_off, const int32_t* label_ids, int32_t n_labels,
+                            float* logprobs, float* lse, void* workspace, size_t ws_bytes,
+                            void* stream);
+
+/* Stable softmax over each branch's labels (openjev-sglang article, request
+ * flow step 5 and the worked yes/no example):
+ *   probs[j] = exp(logprobs[j] - m) / sum_i exp(logprobs[i] - m), m = branch max
+ *   argmax[n] = index (within the branch) of the largest logprob; lowest on ties.
+ *   logprobs  DEVICE fp32 [label_off[N]];  label_off: DEVICE int32 [N+1]
+ *   probs     DEVICE fp32 [label_off[N]];  argmax: DEVICE int32 [N]
+ * Each branch needs 2..64 labels (the article's option limits); otherwise its
+ * outputs are NaN / -1 and SP_ERR_DEVICE_BOUNDS is raised. */
+sp_status sp_label_softmax(const float* logprobs, const int32_t* label_off, int32_t N, float* probs,
+                           int32_t* argmax, void* stream);
+
+/* Host-side validation of a label CSR (HOST arrays): counts in [2, 64],
+ * 0 <= id < vocab, monotone offsets.  SP_OK or SP_ERR_ARG. */
+sp_status sp_check_labels(const int32_t* label_off, const int32_t* label_ids, int32_t N,
+                          int32_t vocab);
+
+/* Synchronise `stream`, read and clear the device error word of the current
+ * device.  SP_OK, SP_ERR_DEVICE_TIMEOUT, SP_ERR_DEVICE_BOUNDS or SP_ERR_CUDA. */
+sp_status sp_check_device_error(void* stream);
+
+const char* sp_status_str(sp_status s);
+
+/* Number of kernel launches the last attention / readout entry point
+ * enqueued on this thread (for launch accounting). */
+int32_t sp_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SP_H_ */

@@ -1,0 +1,203 @@
+// C-ABI entry points that touch the GPU: descriptor upload, the two
+// attention calls, the label readout and softmax, and the device error word.
+// Every argument is validated on the host before anything is launched.
+#include <cstring>
+#include <mutex>
+
+#include "../../include/sp.h"
+#include "common.cuh"
+#include "launch.h"
+#include "plan_internal.h"
+
+namespace {
+
+// Sticky device error word (bits sp::kErrTimeout, sp::kErrBounds).
+__device__ unsigned g_sp_error_word;
+
+constexpr int kMaxDevices = 64;
+thread_local int32_t t_last_launches = 0;
+
+unsigned* error_word_ptr() {
+  static unsigned* ptrs[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_sp_error_word) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<unsigned*>(p);
+  }
+  return ptrs[dev];
+}
+
+int sm_count() {
+  static int counts[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 152;
+  if (!counts[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 152;
+    counts[dev] = n;
+  }
+  return counts[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+sp_status attn_call(const sp_plan* P, const void* dev_desc, int32_t round, int kind, const void* q,
+                    const void* k, const void* v, void* kv_pool, void* out, float* lse,
+                    void* workspace, size_t ws_bytes, void* stream) {
+  t_last_launches = 0;
+  if (!P || !dev_desc || !q || !k || !v || !kv_pool || !out || !lse) return SP_ERR_ARG;
+  if (round < 0 || round >= P->stats.n_rounds) return SP_ERR_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(kv_pool) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(dev_desc) & 255u))
+    return SP_ERR_ARG;
+  const sp_plan::Call& c = P->calls[2 * (size_t)round + kind];
+  const size_t need = (size_t)c.n_parts * P->shape.n_kv_heads * sp::kRowsPerTile *
+                      (P->shape.head_dim + 1) * sizeof(float);
+  if (need > 0 && (!workspace || ws_bytes < need || !aligned16(workspace)))
+    return SP_ERR_WORKSPACE;
+  sp::AttnLaunch L;
+  L.hdr = &P->hdr;
+  L.dev_desc = dev_desc;
+  L.append_off = c.append_off;
+  L.n_append = c.n_append;
+  L.tile_off = c.tile_off;
+  L.n_tiles = c.n_tiles;
+  L.merge_off = c.merge_off;
+  L.n_merges = c.n_merges;
+  L.n_parts = c.n_parts;
+  L.q = q;
+  L.k = k;
+  L.v = v;
+  L.pool = kv_pool;
+  L.out = out;
+  L.lse = lse;
+  L.workspace = workspace;
+  L.Hq = P->shape.n_q_heads;
+  L.Hkv = P->shape.n_kv_heads;
+  L.head_dim = P->shape.head_dim;
+  L.stream = stream;
+  int launches = 0;
+  L.launches = &launches;
+  cudaError_t e = sp::attn_run_call(L);
+  t_last_launches = launches;
+  return e == cudaSuccess ? SP_OK : SP_ERR_CUDA;
+}
+
+}  // namespace
+
+namespace sp {
+EncodeTiledFn get_encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+}  // namespace sp
+
+extern "C" sp_status sp_plan_upload(const sp_plan* plan, void* dev_desc, size_t bytes,
+                                    void* stream) {
+  if (!plan || !dev_desc) return SP_ERR_ARG;
+  if (reinterpret_cast<uintptr_t>(dev_desc) & 255u) return SP_ERR_ARG;
+  if (bytes < plan->blob.size()) return SP_ERR_WORKSPACE;
+  cudaError_t e = cudaMemcpyAsync(dev_desc, plan->blob.data(), plan->blob.size(),
+                                  cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SP_OK : SP_ERR_CUDA;
+}
+
+extern "C" sp_status sp_prefix_attn(const sp_plan* plan, const void* dev_desc, int32_t round,
+                                    const void* q, const void* k, const void* v, void* kv_pool,
+                                    void* out, float* lse, void* workspace, size_t ws_bytes,
+                                    void* stream) {
+  return attn_call(plan, dev_desc, round, 0, q, k, v, kv_pool, out, lse, workspace, ws_bytes,
+                   stream);
+}
+
+extern "C" sp_status sp_branch_attn(const sp_plan* plan, const void* dev_desc, int32_t round,
+                                    const void* q, const void* k, const void* v, void* kv_pool,
+                                    void* out, float* lse, void* workspace, size_t ws_bytes,
+                                    void* stream) {
+  return attn_call(plan, dev_desc, round, 1, q, k, v, kv_pool, out, lse, workspace, ws_bytes,
+                   stream);
+}
+
+extern "C" size_t sp_label_workspace_bytes(int32_t n_branches, int32_t vocab, int32_t n_sms) {
+  if (n_branches <= 0 || vocab < 2) return 0;
+  return sp::lmhead_workspace_bytes(n_branches, vocab, n_sms > 0 ? n_sms : sm_count());
+}
+
+extern "C" sp_status sp_label_logprobs(const void* h, const void* W, int32_t N, int32_t H,
+                                       int32_t V, const int32_t* label_off,
+                                       const int32_t* label_ids, int32_t n_labels, float* logprobs,
+                                       float* lse, void* workspace, size_t ws_bytes,
+                                       void* stream) {
+  t_last_launches = 0;
+  if (!h || !W || !label_off || !logprobs || !lse) return SP_ERR_ARG;
+  if (N < 1 || N > 4096 || H < 8 || H % 8 || V < 2 || n_labels < 0) return SP_ERR_ARG;
+  if (n_labels > 0 && !label_ids) return SP_ERR_ARG;
+  if (!aligned16(h) || !aligned16(W)) return SP_ERR_ARG;
+  const int n_sms = sm_count();
+  const size_t need = sp::lmhead_workspace_bytes(N, V, n_sms);
+  if (!workspace || ws_bytes < need || !aligned16(workspace)) return SP_ERR_WORKSPACE;
+  sp::LmheadLaunch L;
+  L.h = h;
+  L.W = W;
+  L.N = N;
+  L.H = H;
+  L.V = V;
+  L.label_off = label_off;
+  L.label_ids = label_ids;
+  L.n_labels = n_labels;
+  L.logprobs = logprobs;
+  L.lse = lse;
+  L.workspace = workspace;
+  L.ws_bytes = ws_bytes;
+  L.err = error_word_ptr();
+  L.n_sms = n_sms;
+  L.stream = stream;
+  int launches = 0;
+  L.launches = &launches;
+  if (!L.err) return SP_ERR_CUDA;
+  cudaError_t e = sp::lmhead_run(L);
+  t_last_launches = launches;
+  return e == cudaSuccess ? SP_OK : SP_ERR_CUDA;
+}
+
+extern "C" sp_status sp_label_softmax(const float* logprobs, const int32_t* label_off, int32_t N,
+                                      float* probs, int32_t* argmax, void* stream) {
+  t_last_launches = 0;
+  if (!logprobs || !label_off || !probs || !argmax || N < 1) return SP_ERR_ARG;
+  unsigned* err = error_word_ptr();
+  if (!err) return SP_ERR_CUDA;
+  cudaError_t e = sp::label_softmax_run(logprobs, label_off, N, probs, argmax, err, stream);
+  t_last_launches = 1;
+  return e == cudaSuccess ? SP_OK : SP_ERR_CUDA;
+}
+
+extern "C" sp_status sp_check_device_error(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SP_ERR_CUDA;
+  unsigned word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_sp_error_word, sizeof(word)) != cudaSuccess)
+    return SP_ERR_CUDA;
+  if (word) {
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_sp_error_word, &zero, sizeof(zero)) != cudaSuccess)
+      return SP_ERR_CUDA;
+  }
+  if (word & sp::kErrTimeout) return SP_ERR_DEVICE_TIMEOUT;
+  if (word & sp::kErrBounds) return SP_ERR_DEVICE_BOUNDS;
+  return SP_OK;
+}
+
+extern "C" int32_t sp_last_launch_count(void) { return t_last_launches; }

