@@ -174,6 +174,41 @@ extern "C" sp_status sp_label_logprobs(const void* h, const void* W, int32_t N, 
   return e == cudaSuccess ? SP_OK : SP_ERR_CUDA;
 }
 
+extern "C" sp_status sp_label_logprobs_noalloc(const void* h, const void* W, int32_t N, int32_t H,
+                                               int32_t V, const int32_t* label_off,
+                                               const int32_t* label_ids, int32_t n_labels,
+                                               float* logprobs, float* lse, void* stream) {
+  t_last_launches = 0;
+  if (!h || !W || !label_off || !logprobs || !lse) return SP_ERR_ARG;
+  if (N < 1 || H < 8 || H % 8 || V < 2 || n_labels < 0) return SP_ERR_ARG;
+  if (n_labels > 0 && !label_ids) return SP_ERR_ARG;
+  if (!aligned16(h) || !aligned16(W)) return SP_ERR_ARG;
+  if (N > SP_NOALLOC_MAX_BRANCHES) return SP_ERR_WORKSPACE;
+  sp::LmheadLaunch L;
+  L.h = h;
+  L.W = W;
+  L.N = N;
+  L.H = H;
+  L.V = V;
+  L.label_off = label_off;
+  L.label_ids = label_ids;
+  L.n_labels = n_labels;
+  L.logprobs = logprobs;
+  L.lse = lse;
+  L.workspace = nullptr;
+  L.ws_bytes = 0;
+  L.err = error_word_ptr();
+  L.n_sms = sm_count();
+  L.stream = stream;
+  int launches = 0;
+  L.launches = &launches;
+  if (!L.err) return SP_ERR_CUDA;
+  cudaError_t e = sp::lmhead_run_noalloc(L);
+  t_last_launches = launches;
+  if (e == cudaErrorInvalidValue) return SP_ERR_WORKSPACE;
+  return e == cudaSuccess ? SP_OK : SP_ERR_CUDA;
+}
+
 extern "C" sp_status sp_label_softmax(const float* logprobs, const int32_t* label_off, int32_t N,
                                       float* probs, int32_t* argmax, void* stream) {
   t_last_launches = 0;

@@ -49,6 +49,12 @@ struct LmheadLaunch {
 size_t lmhead_workspace_bytes(int N, int V, int n_sms);
 cudaError_t lmhead_run(const LmheadLaunch& L);
 
+// The readout with its scratch in the library's static device array (no
+// allocation); N <= kNoallocMaxBranches.
+constexpr int kNoallocMaxBranches = 1024;
+constexpr int kNoallocMaxCtas = 256;
+cudaError_t lmhead_run_noalloc(LmheadLaunch L);
+
 cudaError_t label_softmax_run(const float* logprobs, const int32_t* label_off, int N, float* probs,
                               int32_t* argmax, unsigned* err, void* stream);
 

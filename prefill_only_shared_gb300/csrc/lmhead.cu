@@ -16,6 +16,8 @@
 //               of TMEM when a label id falls in the tile.
 // A finalize kernel merges the per-CTA (max, sum) pairs into lse and turns
 // the label logits into log-probabilities.
+#include <mutex>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -367,6 +369,50 @@ cudaError_t lmhead_run(const LmheadLaunch& L) {
                                                         L.label_ids, L.logprobs, L.lse, L.err);
   *L.launches = 2;
   return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// No-allocation readout: the per-CTA partials live in this file-scope device
+// array (2 MiB: up to 256 CTAs x 1024 branches x one float2), which every GPU
+// that loads the library holds until exit.  Host code cannot use the array's
+// name as a device address, so its address is looked up once per device (with
+// that device current) and passed to the kernel like any workspace.  Calls
+// share the array; each call writes every partial it reads, so nothing needs
+// clearing, and overlapping calls would race.
+namespace {
+constexpr size_t kNoallocScratchBytes = (size_t)kNoallocMaxCtas * kNoallocMaxBranches * sizeof(float2);
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+cudaError_t noalloc_scratch_address(void** out) {
+  constexpr int kMaxDevices = 64;
+  static void* addr[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t lmhead_run_noalloc(LmheadLaunch L) {
+  if (L.N > kNoallocMaxBranches) return cudaErrorInvalidValue;
+  if (L.n_sms > kNoallocMaxCtas) L.n_sms = kNoallocMaxCtas;  // caps the grid, hence the partials
+  if (lmhead_workspace_bytes(L.N, L.V, L.n_sms) > kNoallocScratchBytes) return cudaErrorInvalidValue;
+  void* scratch = nullptr;
+  cudaError_t e = noalloc_scratch_address(&scratch);
+  if (e != cudaSuccess) return e;
+  L.workspace = scratch;
+  L.ws_bytes = kNoallocScratchBytes;
+  return lmhead_run(L);
 }
 
 // ---------------------------------------------------------------------------

@@ -70,6 +70,7 @@ SIGNATURES = {
     "sp_branch_attn": (_I32, [_P, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "sp_label_workspace_bytes": (_SZ, [_I32, _I32, _I32]),
     "sp_label_logprobs": (_I32, [_P, _P, _I32, _I32, _I32, _P, _P, _I32, _P, _P, _P, _SZ, _P]),
+    "sp_label_logprobs_noalloc": (_I32, [_P, _P, _I32, _I32, _I32, _P, _P, _I32, _P, _P, _P]),
     "sp_label_softmax": (_I32, [_P, _P, _I32, _P, _P, _P]),
     "sp_check_labels": (_I32, [_I32P, _I32P, _I32, _I32]),
     "sp_check_device_error": (_I32, [_P]),
@@ -267,6 +268,22 @@ def sp_label_logprobs(h, W, label_off, label_ids, n_labels: int, logprobs, lse, 
         int(n_labels), _dev(logprobs, torch.float32, "logprobs"), _dev(lse, torch.float32, "lse"),
         _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream))
     _check(st, "sp_label_logprobs")
+
+
+def sp_label_logprobs_noalloc(h, W, label_off, label_ids, n_labels: int, logprobs, lse,
+                              stream=None):
+    """sp_label_logprobs without a workspace: for callers that cannot allocate
+    device memory (the scratch is a static array inside libsp; N <= 1024)."""
+    N, H = h.shape
+    V = W.shape[0]
+    if W.shape[1] != H:
+        raise ValueError("W must be [V, H] with the hidden size of h")
+    st = lib().sp_label_logprobs_noalloc(
+        _dev(h, torch.bfloat16, "h"), _dev(W, torch.bfloat16, "W"), N, H, V,
+        _dev(label_off, torch.int32, "label_off"), _dev(label_ids, torch.int32, "label_ids"),
+        int(n_labels), _dev(logprobs, torch.float32, "logprobs"), _dev(lse, torch.float32, "lse"),
+        _stream(stream))
+    _check(st, "sp_label_logprobs_noalloc")
 
 
 def sp_label_softmax(logprobs, label_off, probs, argmax, stream=None):
