@@ -40,6 +40,10 @@ def parse():
     ap.add_argument("--impl", default="libsp", choices=["libsp", "reference"])
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--schedule", default="rounds", choices=["rounds", "all"],
+                    help="attention calls per staged round, or one call for all rounds")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip the oracle timing (short profiling runs)")
     return ap.parse_args()
 
 
@@ -177,16 +181,19 @@ def run_libsp(args, ws, rank, local):
     stream = torch.cuda.current_stream(dev)
 
     # events around the readout call of every timed step (dominant kernel)
-    def step(ev=None):
+    def step(ev=None, schedule=args.schedule):
         plan = clf.plan(wl.req_of_branch, wl.tok_offsets, wl.tokens)
         if ev is not None:
             ev[0].record(stream)
-        clf.attention(plan, q, k, v, stream)
+        clf.attention(plan, q, k, v, stream, schedule)
         if ev is not None:
             ev[1].record(stream)
-        logprobs, lse, probs, am = clf.readout(h, W, off, ids, n_labels, stream)
+        logprobs, lse = clf.logprobs(h, W, off, ids, n_labels, stream)
         if ev is not None:
             ev[2].record(stream)
+        clf.softmax(logprobs, off, stream)
+        if ev is not None:
+            ev[3].record(stream)
         return plan
 
     plan = step()
@@ -194,7 +201,8 @@ def run_libsp(args, ws, rank, local):
     sp.sp_check_device_error()
     stats = plan.stats()
     segs = plan.segments()
-    launches_per_step = clf.last_launches
+    launches_per_step = clf.last_attention_launches + clf.last_logprob_launches + \
+        clf.last_softmax_launches
     branch_tokens = int(sum(segs["len"][i] for i in range(len(segs["len"])) if not segs["shared"][i]))
     branch_tokens += int(plan.branches()["recompute"].sum())
     f_prefix, f_branch = attention_flops(segs, wl)
@@ -204,7 +212,7 @@ def run_libsp(args, ws, rank, local):
     torch.cuda.synchronize()
 
     # phase events inside the timed region
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_stop = torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
@@ -224,10 +232,26 @@ def run_libsp(args, ws, rank, local):
     total_ms = t_start.elapsed_time(t_stop)
     attn_ms = [e[0].elapsed_time(e[1]) for e in evs]
     lm_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    sm_ms = [e[2].elapsed_time(e[3]) for e in evs]
     if ws > 1:
         t = torch.tensor([total_ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         total_ms = float(t.item())
+    sp.sp_check_device_error()
+
+    # the other attention schedule, same steps, for comparison
+    other = "all" if args.schedule == "rounds" else "rounds"
+    for _ in range(args.warmup):
+        step(schedule=other)
+    torch.cuda.synchronize()
+    o0 = torch.cuda.Event(enable_timing=True)
+    o1 = torch.cuda.Event(enable_timing=True)
+    o0.record(stream)
+    for i in range(args.steps):
+        step(schedule=other)
+    o1.record(stream)
+    torch.cuda.synchronize()
+    other_ms = o0.elapsed_time(o1) / args.steps
     sp.sp_check_device_error()
 
     # ---- end-to-end through the public call, host buffers --------------------
@@ -247,23 +271,25 @@ def run_libsp(args, ws, rank, local):
         for d_, s_ in ((dq, hq), (dk, hk), (dv, hv), (dh, hh), (doff, hoff), (dids, hids)):
             d_.copy_(s_, non_blocking=True)
         res = clf.run(wl.req_of_branch, wl.tok_offsets, wl.tokens, dq, dk, dv, dh, W, doff, dids,
-                      stream)
+                      stream, args.schedule)
         out_probs.copy_(res.probs, non_blocking=True)
         out_am.copy_(res.argmax, non_blocking=True)
 
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    if ws > 1:
-        torch.distributed.barrier()
-    e0.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    e2e_ms = float("nan")
+    if args.e2e_steps > 0:
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        if ws > 1:
+            torch.distributed.barrier()
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
     if ws > 1:
         t = torch.tensor([e2e_ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -301,13 +327,17 @@ def run_libsp(args, ws, rank, local):
             "rounds": stats["n_rounds"],
             "l2": "inputs larger than L2 (the 622 MB LM head is streamed every step)",
             "parallelism": f"replicas x{ws} (independent workloads per GPU)",
+            "attention_schedule": args.schedule,
         },
+        "other_schedule": {"schedule": other, "ms_per_step": round(other_ms, 5),
+                           "value": round(branch_tokens * ws / (other_ms / 1e3), 1)},
         "decisions_per_s": round(N * ws / (ms / 1e3), 1),
         "logical_tokens_per_s": round(stats["logical_tokens"] * ws / (ms / 1e3), 1),
-        "phase_ms": {"attention": round(attn_avg, 5), "readout": round(lm_avg, 5),
-                     "plan_and_launch_overhead": round(ms - attn_avg - lm_avg, 5)},
+        "phase_ms": {"attention": round(attn_avg, 5), "label_logprobs": round(lm_avg, 5),
+                     "label_softmax": round(statistics.mean(sm_ms), 5),
+                     "plan_and_launch_overhead": round(ms - attn_avg - lm_avg - statistics.mean(sm_ms), 5)},
         "roofline": {
-            "kernel": "lmhead_kernel (+ its finalize launch)",
+            "kernel": "lmhead_kernel (sp_label_logprobs: streaming kernel + its finalize launch)",
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peaks["hbm_gbs"],
@@ -333,7 +363,7 @@ def run_libsp(args, ws, rank, local):
         "gpu_launches": int(launches_per_step * args.steps),
         "clocks": clocks,
     }
-    if rank == 0:
+    if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(wl, args.config)
     if ws > 1:
         torch.distributed.destroy_process_group()

@@ -148,7 +148,7 @@ sp_status sp_plan_branches(const sp_plan* plan, const int32_t** branch_last_seg,
 sp_status sp_plan_descriptor(const sp_plan* plan, const void** data, size_t* bytes);
 
 /* Launch lists of one call (kind 0 = sp_prefix_attn, 1 = sp_branch_attn) of
- * `round`: info[0..6] = append offset, appends, tile offset, tiles, merge
+ * `round` (or SP_ALL_ROUNDS): info[0..6] = append offset, appends, tile offset, tiles, merge
  * offset, merges (entries of the descriptor lists), partial slots used. */
 sp_status sp_plan_call_info(const sp_plan* plan, int32_t round, int32_t kind, int64_t info[7]);
 
@@ -156,6 +156,8 @@ sp_status sp_plan_call_info(const sp_plan* plan, int32_t round, int32_t kind, in
  * caller's DEVICE buffer dev_desc (>= 256-byte aligned) on `stream`.  The host
  * source lives in the plan: keep the plan alive until the copy completes. */
 sp_status sp_plan_upload(const sp_plan* plan, void* dev_desc, size_t bytes, void* stream);
+
+#define SP_ALL_ROUNDS (-1)
 
 /* Shared-prefix attention for the segments first computed in `round`.
  *
@@ -168,11 +170,17 @@ sp_status sp_plan_upload(const sp_plan* plan, void* dev_desc, size_t bytes, void
  * 1/sqrt(head_dim), and merge the levels with a log-sum-exp combine.
  *
  *   dev_desc  DEVICE, the uploaded descriptor of this plan
- *   round     0 <= round < n_rounds; calls must run in round order, and the
- *             prefix call of a round before its branch call
+ *   round     0 <= round < n_rounds: the segments first computed in that
+ *             round; calls must run in round order, and the prefix call of a
+ *             round before its branch call.  SP_ALL_ROUNDS (-1): the work of
+ *             every round in one call (the prefix call before the branch
+ *             call); same results, fewer launches for a one-shot pass.
  *   q         DEVICE bf16 [node_tokens, n_q_heads, head_dim]
  *   k, v      DEVICE bf16 [node_tokens, n_kv_heads, head_dim]
- *   kv_pool   DEVICE bf16 [max_pages, 2 (K,V), n_kv_heads, page_size, head_dim]
+ *   kv_pool   DEVICE bf16, per page: K as [n_kv_heads][page_size][head_dim],
+ *             then V transposed as [n_kv_heads][head_dim][page_size]
+ *             (page p starts at element p * 2 * n_kv_heads * page_size * head_dim;
+ *             the pool holds at least stats.pages_used pages)
  *   out       DEVICE bf16 [node_tokens, n_q_heads, head_dim]; rows of this
  *             call's segments are written (round to nearest even)
  *   lse       DEVICE fp32 [node_tokens, n_q_heads]; natural-log sum of exp of

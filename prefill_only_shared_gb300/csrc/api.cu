@@ -51,11 +51,12 @@ sp_status attn_call(const sp_plan* P, const void* dev_desc, int32_t round, int k
                     void* workspace, size_t ws_bytes, void* stream) {
   t_last_launches = 0;
   if (!P || !dev_desc || !q || !k || !v || !kv_pool || !out || !lse) return SP_ERR_ARG;
-  if (round < 0 || round >= P->stats.n_rounds) return SP_ERR_ARG;
+  if (round < -1 || round >= P->stats.n_rounds) return SP_ERR_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(kv_pool) || !aligned16(out) ||
       (reinterpret_cast<uintptr_t>(dev_desc) & 255u))
     return SP_ERR_ARG;
-  const sp_plan::Call& c = P->calls[2 * (size_t)round + kind];
+  const int32_t r = round < 0 ? (int32_t)P->stats.n_rounds : round;
+  const sp_plan::Call& c = P->calls[2 * (size_t)r + kind];
   const size_t need = (size_t)c.n_parts * P->shape.n_kv_heads * sp::kRowsPerTile *
                       (P->shape.head_dim + 1) * sizeof(float);
   if (need > 0 && (!workspace || ws_bytes < need || !aligned16(workspace)))
@@ -80,6 +81,10 @@ sp_status attn_call(const sp_plan* P, const void* dev_desc, int32_t round, int k
   L.Hq = P->shape.n_q_heads;
   L.Hkv = P->shape.n_kv_heads;
   L.head_dim = P->shape.head_dim;
+  L.node_tokens = P->stats.node_tokens;
+  L.pool_pages = P->stats.pages_used;
+  L.err = error_word_ptr();
+  if (!L.err) return SP_ERR_CUDA;
   L.stream = stream;
   int launches = 0;
   L.launches = &launches;

@@ -6,7 +6,7 @@
 namespace sp {
 
 constexpr int kRowsPerTile = 128;  // query rows (token x group-head) per CTA tile
-constexpr int kKeysPerUnit = 64;   // keys per KV unit (4 pages of 16)
+constexpr int kKeysPerUnit = 128;  // keys per KV unit (8 pages of 16): one MMA N tile
 constexpr int kPageSize = 16;      // tokens per KV page
 
 // One trie segment.  Its K/V live in pages page_ids[page_off ..]; its
@@ -24,10 +24,11 @@ struct SegDesc {
 // query heads of one KV head, which is the launch's y index), over the KV
 // units [u_lo, u_hi) of its context (ancestor units first, then own units up
 // to the causal bound).  part < 0: write final out/lse; else write partial
-// slot `part` for the merge kernel.
+// slot `part`; the last of the split tile's parts to finish (merge entry
+// `merge` of the call) combines them.
 struct TileDesc {
   int32_t seg, t0, nt, u_lo, u_hi, part;
-  int32_t pad0, pad1;
+  int32_t merge, pad1;
 };
 
 // Rows of one split tile whose `nparts` partials start at slot part0.

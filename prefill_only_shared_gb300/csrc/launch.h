@@ -22,6 +22,9 @@ struct AttnLaunch {
   float* lse;
   void* workspace;
   int Hq, Hkv, head_dim;
+  int64_t node_tokens;  // rows of q/out (bounds the Q tensor map)
+  int64_t pool_pages;   // pages the plan uses (bounds the pool tensor maps)
+  unsigned* err;
   void* stream;
   int* launches;
 };

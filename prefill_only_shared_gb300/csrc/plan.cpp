@@ -298,20 +298,25 @@ extern "C" sp_status sp_plan_build(const sp_shape* shape, int32_t n_branches,
   const int32_t G = shape->n_q_heads / shape->n_kv_heads;
   const int32_t TPT = sp::kRowsPerTile / G;
   const int32_t Hkv = shape->n_kv_heads;
-  const int64_t part_target = std::max<int64_t>(1, (2 * (int64_t)P->n_sms + Hkv - 1) / Hkv);
+  // one attention CTA per SM (the kernel holds all 512 TMEM columns)
+  const int64_t part_target = std::max<int64_t>(1, ((int64_t)P->n_sms + Hkv - 1) / Hkv);
   std::vector<sp::AppendDesc> appends;
   std::vector<sp::TileDesc> tiles;
   std::vector<sp::MergeDesc> merges;
   int64_t max_parts = 0;
-  P->calls.resize(2 * (size_t)n_rounds);
-  for (int32_t r = 0; r < n_rounds; ++r) {
+  // calls[2 r + kind] for rounds r < n_rounds; calls[2 n_rounds + kind] run the
+  // work of every round in one call (valid because a call appends all of its
+  // segments' K/V before any of its attention runs).
+  P->calls.resize(2 * (size_t)n_rounds + 2);
+  for (int32_t r = 0; r <= n_rounds; ++r) {
+    const bool all = r == n_rounds;
     for (int kind = 0; kind < 2; ++kind) {
       sp_plan::Call& call = P->calls[2 * r + kind];
       struct Raw { int32_t seg, t0, nt; int64_t units; };
       std::vector<Raw> raw;
       call.append_off = (int64_t)appends.size();
       for (int32_t s = 0; s < S; ++s) {
-        if (P->seg_round[s] != r) continue;
+        if (!all && P->seg_round[s] != r) continue;
         if ((kind == 0) != (P->seg_shared[s] != 0)) continue;
         for (int32_t pg = 0; pg < ceil_div(P->seg_len[s], sp::kPageSize); ++pg)
           appends.push_back({s, pg});
@@ -321,8 +326,9 @@ extern "C" sp_status sp_plan_build(const sp_shape* shape, int32_t n_branches,
         }
       }
       if (kind == 1) {
-        for (int32_t i = P->round_off[r]; i < P->round_off[r + 1]; ++i) {
-          int32_t b = P->round_branches[i];
+        const int32_t i0 = all ? 0 : P->round_off[r], i1 = all ? N : P->round_off[r + 1];
+        for (int32_t i = i0; i < i1; ++i) {
+          int32_t b = all ? i : P->round_branches[i];
           if (!P->branch_recompute[b]) continue;
           int32_t s = P->branch_last_seg[b];
           int32_t t0 = P->seg_len[s] - 1;
@@ -340,14 +346,15 @@ extern "C" sp_status sp_plan_build(const sp_shape* shape, int32_t n_branches,
       int32_t parts = 0;
       for (auto& x : raw) {
         if (x.units <= budget) {
-          work.push_back({{x.seg, x.t0, x.nt, 0, (int32_t)x.units, -1, 0, 0}, x.units});
+          work.push_back({{x.seg, x.t0, x.nt, 0, (int32_t)x.units, -1, -1, 0}, x.units});
           continue;
         }
         int32_t np = (int32_t)ceil_div(x.units, budget);
+        const int32_t mi = (int32_t)(merges.size() - call.merge_off);  // index within the call
         merges.push_back({x.seg, x.t0, x.nt, parts, np, 0, 0, 0});
         for (int32_t i = 0; i < np; ++i) {
           int32_t lo = (int32_t)(x.units * i / np), hi = (int32_t)(x.units * (i + 1) / np);
-          work.push_back({{x.seg, x.t0, x.nt, lo, hi, parts + i, 0, 0}, (int64_t)(hi - lo)});
+          work.push_back({{x.seg, x.t0, x.nt, lo, hi, parts + i, mi, 0}, (int64_t)(hi - lo)});
         }
         parts += np;
       }
@@ -407,9 +414,10 @@ extern "C" sp_status sp_plan_build(const sp_shape* shape, int32_t n_branches,
   P->stats.computed_tokens = P->stats.node_tokens + recomputed;
   P->stats.reused_tokens = logical - P->stats.computed_tokens;
   P->stats.desc_bytes = (int64_t)P->blob.size();
-  P->stats.attn_workspace_bytes =
-      (int64_t)align256((size_t)std::max<int64_t>(max_parts, 1) * Hkv * sp::kRowsPerTile *
-                        (shape->head_dim + 1) * sizeof(float));
+  // partial O and lse per split part
+  P->stats.attn_workspace_bytes = (int64_t)align256(
+      (size_t)std::max<int64_t>(max_parts, 1) * Hkv * sp::kRowsPerTile * (shape->head_dim + 1) *
+      sizeof(float));
   *out = P;
   return SP_OK;
 }
@@ -473,9 +481,10 @@ extern "C" sp_status sp_plan_descriptor(const sp_plan* plan, const void** data, 
 
 extern "C" sp_status sp_plan_call_info(const sp_plan* plan, int32_t round, int32_t kind,
                                        int64_t info[7]) {
-  if (!plan || !info || round < 0 || round >= plan->stats.n_rounds || kind < 0 || kind > 1)
+  if (!plan || !info || round < -1 || round >= plan->stats.n_rounds || kind < 0 || kind > 1)
     return SP_ERR_ARG;
-  const sp_plan::Call& c = plan->calls[2 * (size_t)round + kind];
+  const int32_t r = round < 0 ? (int32_t)plan->stats.n_rounds : round;
+  const sp_plan::Call& c = plan->calls[2 * (size_t)r + kind];
   info[0] = c.append_off;
   info[1] = c.n_append;
   info[2] = c.tile_off;

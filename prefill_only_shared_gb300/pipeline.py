@@ -65,7 +65,10 @@ class SharedPrefixClassifier:
         self._ensure_pool(plan.stats()["pages_used"])
         return plan
 
-    def attention(self, plan, q, k, v, stream=None):
+    def attention(self, plan, q, k, v, stream=None, schedule="rounds"):
+        """schedule "rounds": one prefix and one branch call per staged round,
+        in round order; "all": one prefix call and one branch call covering
+        every round (same results, fewer launches)."""
         st = plan.stats()
         T = st["node_tokens"]
         Hq, d = self.shape.n_q_heads, self.shape.head_dim
@@ -77,7 +80,8 @@ class SharedPrefixClassifier:
         out = self._buf("out", T * Hq * d, torch.bfloat16).view(T, Hq, d)
         lse = self._buf("lse", T * Hq, torch.float32).view(T, Hq)
         launches = 0
-        for r in range(st["n_rounds"]):
+        rounds = range(st["n_rounds"]) if schedule == "rounds" else [sp.SP_ALL_ROUNDS]
+        for r in rounds:
             sp.sp_prefix_attn(plan, desc, r, q, k, v, self.kv_pool, out, lse, ws, stream)
             launches += sp.sp_last_launch_count()
             sp.sp_branch_attn(plan, desc, r, q, k, v, self.kv_pool, out, lse, ws, stream)
@@ -85,28 +89,39 @@ class SharedPrefixClassifier:
         self.last_attention_launches = launches
         return out, lse
 
-    def readout(self, h, W, label_off, label_ids, n_labels, stream=None):
+    def logprobs(self, h, W, label_off, label_ids, n_labels, stream=None):
         N = h.shape[0]
         ws = self._buf("lm_ws", sp.sp_label_workspace_bytes(N, W.shape[0], self.n_sms), torch.uint8)
         logprobs = self._buf("logprobs", n_labels, torch.float32)
         lse = self._buf("lse_vocab", N, torch.float32)
         sp.sp_label_logprobs(h, W, label_off, label_ids, n_labels, logprobs, lse, ws, stream)
-        launches = sp.sp_last_launch_count()
-        probs = self._buf("probs", n_labels, torch.float32)
+        self.last_logprob_launches = sp.sp_last_launch_count()
+        return logprobs, lse
+
+    def softmax(self, logprobs, label_off, stream=None):
+        N = label_off.numel() - 1
+        probs = self._buf("probs", logprobs.numel(), torch.float32)
         argmax = self._buf("argmax", N, torch.int32)
         sp.sp_label_softmax(logprobs, label_off, probs, argmax, stream)
-        self.last_readout_launches = launches + sp.sp_last_launch_count()
+        self.last_softmax_launches = sp.sp_last_launch_count()
+        return probs, argmax
+
+    def readout(self, h, W, label_off, label_ids, n_labels, stream=None):
+        logprobs, lse = self.logprobs(h, W, label_off, label_ids, n_labels, stream)
+        probs, argmax = self.softmax(logprobs, label_off, stream)
+        self.last_readout_launches = self.last_logprob_launches + self.last_softmax_launches
         return logprobs, lse, probs, argmax
 
     def run(self, req_of_branch, tok_offsets, tokens, q, k, v, h, W, label_off, label_ids,
-            stream=None) -> PassOutputs:
+            stream=None, schedule="rounds") -> PassOutputs:
         """q/k/v in node-token order of the plan (see sp_plan_segments)."""
         plan = self.plan(req_of_branch, tok_offsets, tokens)
-        out, lse = self.attention(plan, q, k, v, stream)
+        out, lse = self.attention(plan, q, k, v, stream, schedule)
         n_labels = int(label_ids.numel())
         logprobs, lse_v, probs, argmax = self.readout(h, W, label_off, label_ids, n_labels, stream)
         return PassOutputs(out, lse, logprobs, lse_v, probs, argmax, plan)
 
     @property
     def last_launches(self) -> int:
-        return getattr(self, "last_attention_launches", 0) + getattr(self, "last_readout_launches", 0)
+        return (getattr(self, "last_attention_launches", 0) + getattr(self, "last_logprob_launches", 0)
+                + getattr(self, "last_softmax_launches", 0))

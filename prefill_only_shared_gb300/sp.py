@@ -19,6 +19,7 @@ import torch
 from . import build as _build
 
 SP_OK = 0
+SP_ALL_ROUNDS = -1
 STATUS_NAMES = {0: "SP_OK", 1: "SP_ERR_ARG", 2: "SP_ERR_LIMIT", 3: "SP_ERR_POOL_FULL",
                 4: "SP_ERR_CUDA", 5: "SP_ERR_DEVICE_TIMEOUT", 6: "SP_ERR_DEVICE_BOUNDS",
                 7: "SP_ERR_WORKSPACE"}

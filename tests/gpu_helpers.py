@@ -21,7 +21,7 @@ TOL_P = 1e-3
 ARGMAX_MARGIN = 1e-2
 
 
-def run_gpu(wl, stream=None):
+def run_gpu(wl, stream=None, schedule="rounds"):
     from prefill_only_shared_gb300 import sp
     from prefill_only_shared_gb300.pipeline import SharedPrefixClassifier
     dev = torch.device("cuda:0")
@@ -32,7 +32,8 @@ def run_gpu(wl, stream=None):
     h, W = wl.h.to(dev), wl.W.to(dev)
     off = torch.from_numpy(wl.label_off).to(dev)
     ids = torch.from_numpy(wl.label_ids).to(dev)
-    res = clf.run(wl.req_of_branch, wl.tok_offsets, wl.tokens, q, k, v, h, W, off, ids, stream)
+    res = clf.run(wl.req_of_branch, wl.tok_offsets, wl.tokens, q, k, v, h, W, off, ids, stream,
+                  schedule)
     torch.cuda.synchronize()
     sp.sp_check_device_error()
     return {

@@ -43,12 +43,13 @@ SMALL = [
 ]
 
 
+@pytest.mark.parametrize("schedule", ["rounds", "all"])
 @pytest.mark.parametrize("case", range(len(SMALL)))
-def test_small_ragged_cases(cuda_dev, lib, case):
+def test_small_ragged_cases(cuda_dev, lib, case, schedule):
     trees, Hq, Hkv, d, H, V, labels = SMALL[case]
     wl = small_case(trees, seed=case, n_q_heads=Hq, n_kv_heads=Hkv, head_dim=d, hidden=H,
                     vocab=V, labels=labels)
-    g = run_gpu(wl)
+    g = run_gpu(wl, schedule=schedule)
     check_attention_full(wl, g)
     check_readout(wl, g)
 
@@ -73,18 +74,20 @@ def test_recomputed_final_rows(cuda_dev, lib):
     v = torch.randn(T, 2, 64, generator=gen).bfloat16()
     clf = SharedPrefixClassifier(8, 2, 64, 64, 100, device=cuda_dev)
     plan = clf.plan(req, off, toks)
-    out, lse = clf.attention(plan, q.cuda(), k.cuda(), v.cuda())
-    torch.cuda.synchronize()
-    sp.sp_check_device_error()
     ro, rl, _ = OA.reference_attention(ref, q, k, v)
-    assert np.abs(out.float().cpu().numpy() - ro).max() <= TOL_OUT
-    assert np.abs(lse.cpu().numpy() - rl).max() <= TOL_LSE
+    for schedule in ("rounds", "all"):
+        out, lse = clf.attention(plan, q.cuda(), k.cuda(), v.cuda(), schedule=schedule)
+        torch.cuda.synchronize()
+        sp.sp_check_device_error()
+        assert np.abs(out.float().cpu().numpy() - ro).max() <= TOL_OUT
+        assert np.abs(lse.cpu().numpy() - rl).max() <= TOL_LSE
 
 
+@pytest.mark.parametrize("schedule", ["rounds", "all"])
 @pytest.mark.parametrize("name", ["yesno", "tree2", "choice64"])
-def test_full_size_configs(cuda_dev, lib, name):
+def test_full_size_configs(cuda_dev, lib, name, schedule):
     wl = workload(name)
-    g = run_gpu(wl)
+    g = run_gpu(wl, schedule=schedule)
     expected = {"yesno": [[0], [1, 2, 3, 4]], "tree2": [[0], [1, 2, 3], [4, 5]],
                 "choice64": [[0], list(range(1, 64))]}[name]
     assert g["rounds"] == expected

@@ -19,11 +19,11 @@ from test_oracle_staging import csr, random_case
 SEG = np.dtype([("node_start", "<i8"), ("len", "<i4"), ("page_off", "<i4"), ("chain_off", "<i4"),
                 ("chain_len", "<i4"), ("p0", "<i4"), ("p1", "<i4")])
 TILE = np.dtype([("seg", "<i4"), ("t0", "<i4"), ("nt", "<i4"), ("u_lo", "<i4"), ("u_hi", "<i4"),
-                 ("part", "<i4"), ("p0", "<i4"), ("p1", "<i4")])
+                 ("part", "<i4"), ("merge", "<i4"), ("p1", "<i4")])
 MERGE = np.dtype([("seg", "<i4"), ("t0", "<i4"), ("nt", "<i4"), ("part0", "<i4"), ("nparts", "<i4"),
                   ("p0", "<i4"), ("p1", "<i4"), ("p2", "<i4")])
 APP = np.dtype([("seg", "<i4"), ("page", "<i4")])
-ROWS, UNIT, PAGE = 128, 64, 16
+ROWS, UNIT, PAGE = 128, 128, 16
 
 
 def decode(blob):
@@ -38,7 +38,7 @@ def decode(blob):
             arr("tiles", TILE), arr("merges", MERGE))
 
 
-def emulate(plan, q, k, v, Hq, Hkv, d):
+def emulate(plan, q, k, v, Hq, Hkv, d, schedule="rounds"):
     segs, pages, chain, app, tiles, merges = decode(plan.descriptor())
     st = plan.stats()
     G = Hq // Hkv
@@ -48,7 +48,7 @@ def emulate(plan, q, k, v, Hq, Hkv, d):
     lse = np.full((T, Hq), np.nan)
     scale = 1.0 / math.sqrt(d)
     seen = np.zeros(T, dtype=np.int64)
-    for r in range(st["n_rounds"]):
+    for r in (range(st["n_rounds"]) if schedule == "rounds" else [-1]):
         for kind in (0, 1):
             ci = plan.call_info(r, kind)
             for a in app[ci["append_off"]:ci["append_off"] + ci["n_append"]]:
@@ -62,8 +62,15 @@ def emulate(plan, q, k, v, Hq, Hkv, d):
                     else:
                         pool[pg, :, :, slot] = 0.0
             parts = {}
+            call_merges = merges[ci["merge_off"]:ci["merge_off"] + ci["n_merges"]]
             for td in tiles[ci["tile_off"]:ci["tile_off"] + ci["n_tiles"]]:
                 s = segs[td["seg"]]
+                if td["part"] >= 0:  # a split part names its merge entry
+                    md = call_merges[td["merge"]]
+                    assert md["part0"] <= td["part"] < md["part0"] + md["nparts"]
+                    assert (md["seg"], md["t0"], md["nt"]) == (td["seg"], td["t0"], td["nt"])
+                else:
+                    assert td["merge"] == -1
                 levels = [segs[c] for c in chain[s["chain_off"]:s["chain_off"] + s["chain_len"]]]
                 lv = [(x["page_off"], x["len"], False) for x in levels]
                 lv.append((s["page_off"], td["t0"] + td["nt"], True))
@@ -114,16 +121,17 @@ def check(req, offs, toks, q, k, v, Hq, Hkv, d, lib, n_sms):
     plan = lib.sp_plan_build(lib.make_shape(Hq, Hkv, d, 16, 64, 1000), req, offs, toks, 1 << 20,
                              n_sms=n_sms)
     ref = S.build_plan(req, offs, toks)
-    out, lse, seen = emulate(plan, q, k, v, Hq, Hkv, d)
     ro, rl, _ = A.reference_attention(ref, q, k, v)
-    assert np.abs(out - ro).max() < 1e-10
-    assert np.abs(lse - rl).max() < 1e-10
-    # every row written once, plus one more for each recomputed final row
-    extra = np.zeros_like(seen)
-    for b in range(len(ref.paths)):
-        if ref.recompute[b]:
-            extra[ref.branch_last_row(b)] += 1
-    assert (seen == 1 + extra).all()
+    for schedule in ("rounds", "all"):
+        out, lse, seen = emulate(plan, q, k, v, Hq, Hkv, d, schedule)
+        assert np.abs(out - ro).max() < 1e-10
+        assert np.abs(lse - rl).max() < 1e-10
+        # every row written once, plus one more for each recomputed final row
+        extra = np.zeros_like(seen)
+        for b in range(len(ref.paths)):
+            if ref.recompute[b]:
+                extra[ref.branch_last_row(b)] += 1
+        assert (seen == 1 + extra).all()
     return plan
 
 
