@@ -178,7 +178,7 @@ sp_status sp_plan_upload(const sp_plan* plan, void* dev_desc, size_t bytes, void
  *   q         DEVICE bf16 [node_tokens, n_q_heads, head_dim]
  *   k, v      DEVICE bf16 [node_tokens, n_kv_heads, head_dim]
  *   kv_pool   DEVICE bf16, per page: K as [n_kv_heads][page_size][head_dim],
- *             then V transposed as [n_kv_heads][head_dim][page_size]
+ *             then V as [n_kv_heads][page_size][head_dim]
  *             (page p starts at element p * 2 * n_kv_heads * page_size * head_dim;
  *             the pool holds at least stats.pages_used pages)
  *   out       DEVICE bf16 [node_tokens, n_q_heads, head_dim]; rows of this

@@ -5,28 +5,34 @@
 // prefill reuses the prefix KV and computes only its own suffix), and the
 // LLM2Jev "shared prefix" page (branches continue from the cached prefix).
 //
-// Work unit (one CTA): 128 query rows = (128 / G) consecutive tokens of one
-// segment x the G query heads of one KV head (grouped-query packing: every KV
-// tile loaded into shared memory serves all G heads).  The CTA walks the KV of
-// the segment's ancestors (all keys visible) and then its own keys up to the
-// causal bound, 128 keys (eight 16-token pages) per step.  Long contexts are
-// split over several CTAs whose partial (O, lse) are merged by a log-sum-exp
-// combine in a separate, fully parallel kernel (one warp per row).
+// Work unit (one CTA): 256 query rows = (256 / G) consecutive tokens of one
+// segment x the G query heads of one KV head, as two 128-row halves A and B
+// (grouped-query packing: every KV tile in shared memory serves 2 x 128 rows,
+// which halves the L2 bytes per flop against one 128-row tile).  The CTA walks
+// the KV of the segment's ancestors (all keys visible) and then its own keys
+// up to the causal bound, 128 keys (eight 16-token pages) per step, starting at
+// a rotated step so CTAs sharing a prefix spread their reads.  Long contexts
+// are split over several CTAs whose partial (O, lse) are merged by a
+// log-sum-exp combine in a separate, fully parallel kernel.
 //
-// Roles (192 threads, one CTA per SM):
-//   warps 0..3  softmax: one query row per thread (= TMEM lane); read S from
-//               TMEM, mask, online max with lazy rescaling (the running max is
-//               only moved when it grows by more than 2^8), P = exp2(S - m) in
-//               bf16 into 128B-swizzled shared memory, rescale O in TMEM when
-//               the max moved, final normalisation and store;
-//   warp 4      TMA producer: Q tile once (3-D box: 64 dims x G heads x
-//               128/G tokens), then per step eight K pages (128B swizzle) and
-//               eight transposed V pages (32B swizzle) into a 2-stage ring,
-//               lane p issuing page p, page ids fetched one step ahead;
-//   warp 5      MMA issuer: S = Q K^T (M 128, N 128, K d) into one of two TMEM
-//               buffers, then O += P V (M 128, N d, K 16 per page) into TMEM.
-// The QK product of step j+1 runs on the tensor pipe while the softmax of
-// step j runs.
+// Roles (352 threads, one CTA per SM):
+//   warps 0..3 / 4..7  softmax of half A / half B: one query row per thread
+//               (= TMEM lane); S from TMEM, mask, online max with lazy
+//               rescaling (the running max only moves when it grows by more
+//               than 2^8), row sums in fp32, P = exp2(S - m) written back as
+//               bf16 pairs over the first 64 columns of S in TMEM, rescale of
+//               O in TMEM when the max moved, final normalisation and store;
+//   warp 8      TMA producer of Q (3-D boxes: 64 dims x G heads x 128/G
+//               tokens per half) and of the K pages (128B swizzle, 3 stages);
+//   warp 10     TMA producer of the V pages (128B swizzle, 2 stages); a unit
+//               whose eight page ids are consecutive comes in one 4-D box per
+//               64-dim slab, otherwise one box per page and slab;
+//   warp 9      MMA issuer, in tensor-pipe order per unit j: PV_A(j-1),
+//               QK_A(j), PV_B(j-1), QK_B(j) with S_h = Q_h K^T (M 128, N 128,
+//               K d, operands in shared memory) and O_h += P_h V (M 128, N d,
+//               K 16 per page, P_h read from TMEM, V an MN-major operand).
+// The two halves alternate on the tensor pipe, so one half's softmax runs
+// while the other half's products do.
 #include "common.cuh"
 #include "desc.h"
 #include "launch.h"
@@ -36,28 +42,26 @@ namespace {
 
 using bf16 = __nv_bfloat16;
 
-constexpr int kThreads = 224;  // 4 softmax warps, K producer, MMA issuer, V producer
-constexpr int kKStages = 2;
+constexpr int kThreads = 352;
+constexpr int kHalf = 128;                        // rows per half tile (MMA M)
+constexpr int kKStages = 3;
 constexpr int kVStages = 2;
 constexpr int kPages = kKeysPerUnit / kPageSize;  // pages per unit
 constexpr float kRescaleLog2 = 8.f;  // move the running max only when it grows by > 2^8
 
-// The PV product runs with N = D + 16: each transposed V page carries 16
-// extra rows, the first all ones, so column D of O accumulates the row sum
-// of the same bf16 P that weights V (the softmax denominator).
 template <int D>
 struct Cfg {
-  static constexpr int kVRows = D + 16;                  // rows of a transposed V page block
-  static constexpr int kQ = kRowsPerTile * D * 2;        // Q tile, slabs of 64 dims
-  static constexpr int kK = kKeysPerUnit * D * 2;        // K tile
-  static constexpr int kVPage = kVRows * 32;             // one transposed V page (16 keys)
-  static constexpr int kV = kPages * kVPage;             // V^T tile
-  static constexpr int kP = kRowsPerTile * kKeysPerUnit * 2;  // P tile, 2 slabs of 64 keys
-  static constexpr int kSlab = kRowsPerTile * 128;       // one 64-wide bf16 slab of 128 rows
+  static constexpr int kQSlab = kHalf * 128;             // [128 rows x 64 dims] bf16
+  static constexpr int kQHalf = (D / 64) * kQSlab;       // one half's Q tile
+  static constexpr int kKSlab = kKeysPerUnit * 128;      // [128 keys x 64 dims] bf16
+  static constexpr int kK = (D / 64) * kKSlab;           // K tile of one unit
+  static constexpr int kV = (D / 64) * kKSlab;           // V tile of one unit (like K)
   static constexpr size_t kSmem =
-      1024 + kQ + kP + (size_t)kKStages * kK + (size_t)kVStages * kV + 256;
-  static constexpr uint32_t kColO = 2 * kKeysPerUnit;    // TMEM: S0 | S1 | O (D + 16 columns)
-  static constexpr uint32_t kColSum = kColO + D;         // row sum of P
+      1024 + 2 * kQHalf + (size_t)kKStages * kK + (size_t)kVStages * kV + 512;
+  // TMEM columns: S_A | S_B (128 each; P_h overwrites the first 64 columns of
+  // S_h as packed bf16 pairs) | O_A | O_B (D each)
+  static constexpr uint32_t kColS = 0;
+  static constexpr uint32_t kColO = 2 * kKeysPerUnit;
 };
 
 struct AttnArgs {
@@ -74,15 +78,17 @@ struct AttnArgs {
   float scale_log2;  // log2(e) / sqrt(d)
 };
 
-// K-major operand, 32-byte swizzle: rows of 32 bytes (16 bf16 of K), 8-row
-// groups 256 bytes apart, swizzle mode 6 = 32B.
-__device__ __forceinline__ uint64_t umma_desc_k_sw32(uint32_t smem_addr) {
+// MN-major operand, 128-byte swizzle (V as the B operand of P.V: rows are
+// keys = K, 128-byte rows hold 64 consecutive head dims = N): 8-row K groups
+// 1024 bytes apart (stride byte offset), 64-column N slabs `slab_bytes` apart
+// (leading byte offset), swizzle mode 2 = 128B.
+__device__ __forceinline__ uint64_t umma_desc_mn_sw128(uint32_t smem_addr, uint32_t slab_bytes) {
   uint64_t d = 0;
   d |= (uint64_t)((smem_addr >> 4) & 0x3FFFu);
-  d |= (uint64_t)(16u >> 4) << 16;
-  d |= (uint64_t)(256u >> 4) << 32;
+  d |= (uint64_t)((slab_bytes >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)(1024u >> 4) << 32;
   d |= (uint64_t)1 << 46;
-  d |= (uint64_t)6 << 61;
+  d |= (uint64_t)2 << 61;
   return d;
 }
 
@@ -92,6 +98,15 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int32_t x, int32_t y, int32_t z, int32_t w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w)
       : "memory");
 }
 
@@ -122,6 +137,39 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
       : "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 32 lanes x 128 columns in one load, one wait.
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[128]) {
+  uint32_t r[128];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x128.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%128];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]), "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]), "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]), "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]), "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]), "=r"(r[96]), "=r"(r[97]), "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]), "=r"(r[104]), "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]), "=r"(r[110]), "=r"(r[111]), "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]), "=r"(r[116]), "=r"(r[117]), "=r"(r[118]), "=r"(r[119]), "=r"(r[120]), "=r"(r[121]), "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 128; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 32 lanes x 64 columns stored in one instruction, then wait.
+__device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&w)[64]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]), "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15]), "r"(w[16]), "r"(w[17]), "r"(w[18]), "r"(w[19]), "r"(w[20]), "r"(w[21]), "r"(w[22]), "r"(w[23]), "r"(w[24]), "r"(w[25]), "r"(w[26]), "r"(w[27]), "r"(w[28]), "r"(w[29]), "r"(w[30]), "r"(w[31]), "r"(w[32]), "r"(w[33]), "r"(w[34]), "r"(w[35]), "r"(w[36]), "r"(w[37]), "r"(w[38]), "r"(w[39]), "r"(w[40]), "r"(w[41]), "r"(w[42]), "r"(w[43]), "r"(w[44]), "r"(w[45]), "r"(w[46]), "r"(w[47]), "r"(w[48]), "r"(w[49]), "r"(w[50]), "r"(w[51]), "r"(w[52]), "r"(w[53]), "r"(w[54]), "r"(w[55]), "r"(w[56]), "r"(w[57]), "r"(w[58]), "r"(w[59]), "r"(w[60]), "r"(w[61]), "r"(w[62]), "r"(w[63])
+      : "memory");
+}
+
+// D (TMEM) += A (TMEM: lane = row, 32-bit column c = bf16 pair of K elements
+// 2c, 2c+1) x B (shared-memory descriptor).
+__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
@@ -170,6 +218,31 @@ __device__ __forceinline__ void tmem_st1_sync(uint32_t taddr, float v) {
       : "memory");
 }
 
+// Packed fp32 pairs (Blackwell f32x2 arithmetic) and a three-input maximum.
+__device__ __forceinline__ uint64_t f2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void uf2(uint64_t r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t fma_f2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add_f2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float m;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(m) : "f"(a), "f"(b), "f"(c));
+  return m;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -214,14 +287,36 @@ __device__ __forceinline__ void cursor_next(Cursor& c, const AttnArgs& a, const 
 }
 
 __device__ __forceinline__ Cursor cursor_at(const AttnArgs& a, const SegDesc& sd,
-                                            const TileDesc& td) {
+                                            const TileDesc& td, int unit) {
   Cursor c;
   c.level = 0;
   c.j = 0;
   cursor_level(c, a, sd, td);
-  for (int u = 0; u < td.u_lo; ++u) cursor_next(c, a, sd, td);
+  for (int u = 0; u < unit; ++u) cursor_next(c, a, sd, td);
   return c;
 }
+
+// A CTA walks its units [u_lo, u_hi) starting at a rotated position and
+// wrapping around, so the CTAs that share a prefix do not all request the
+// same KV lines at the same moment.  The online softmax does not depend on
+// the order of the units.
+struct UnitWalk {
+  Cursor cur;
+  int u;
+  __device__ __forceinline__ void start(const AttnArgs& a, const SegDesc& sd, const TileDesc& td) {
+    const int n = td.u_hi - td.u_lo;
+    u = td.u_lo + (int)((blockIdx.x * 5u + blockIdx.y * 3u) % (unsigned)(n > 0 ? n : 1));
+    cur = cursor_at(a, sd, td, u);
+  }
+  __device__ __forceinline__ void next(const AttnArgs& a, const SegDesc& sd, const TileDesc& td) {
+    if (++u == td.u_hi) {
+      u = td.u_lo;
+      cur = cursor_at(a, sd, td, u);
+    } else {
+      cursor_next(cur, a, sd, td);
+    }
+  }
+};
 
 __device__ __forceinline__ unsigned char* align1024(unsigned char* p) {
   return reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(p) + 1023) &
@@ -230,27 +325,25 @@ __device__ __forceinline__ unsigned char* align1024(unsigned char* p) {
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV, AttnArgs a) {
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKr,
+                   const __grid_constant__ CUtensorMap tmK1, const __grid_constant__ CUtensorMap tmVr,
+                   const __grid_constant__ CUtensorMap tmV1, AttnArgs a) {
   using C = Cfg<D>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = align1024(smem_raw);
-  unsigned char* sQ = smem;
-  unsigned char* sP = sQ + C::kQ;
-  unsigned char* sK = sP + C::kP;
-  unsigned char* sV = sK + kKStages * C::kK;
+  unsigned char* sQ = smem;                        // [2 halves][D/64 slabs][128 x 128 B]
+  unsigned char* sK = sQ + 2 * C::kQHalf;          // [stages][D/64 slabs][128 x 128 B]
+  unsigned char* sV = sK + kKStages * C::kK;       // [stages][8 pages][D x 32 B]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sV + kVStages * C::kV);
   uint64_t* q_full = bars;
   uint64_t* k_full = q_full + 1;
   uint64_t* k_empty = k_full + kKStages;
   uint64_t* v_full = k_empty + kKStages;
   uint64_t* v_empty = v_full + kVStages;
-  uint64_t* s_full = v_empty + kVStages;
-  uint64_t* s_empty = s_full + 2;
-  uint64_t* p_full = s_empty + 2;
-  uint64_t* pv_done = p_full + 1;
-  uint64_t* drain = pv_done + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* s_full = v_empty + kVStages;  // [2]: S_h of the current unit is in TMEM
+  uint64_t* p_full = s_full + 2;          // [2]: P_h of the current unit is in TMEM
+  uint64_t* o_full = p_full + 2;          // all products done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_full + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const TileDesc td = a.tiles[blockIdx.x];
@@ -258,6 +351,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const SegDesc sd = a.segs[td.seg];
   const int n_units = td.u_hi - td.u_lo;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = a.G;
+  const bool has_b = td.nt > kHalf / G;  // half B holds at least one token
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -269,25 +364,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&s_full[b], 1);
-      mbar_init(&s_empty[b], 128);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(&s_full[h], 1);
+      mbar_init(&p_full[h], 128);
     }
-    mbar_init(p_full, 128);
-    mbar_init(pv_done, 1);
-    mbar_init(drain, 1);
+    mbar_init(o_full, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  // constant rows of every V page block: row D all ones, rows D+1.. zero
-  for (int i = threadIdx.x; i < kVStages * kPages * 16 * 2; i += blockDim.x) {
-    const int half = i & 1, row = (i >> 1) & 15, blk = i >> 5;
-    const uint32_t one = row == 0 ? 0x3F803F80u : 0u;  // bf16 1.0 pairs
-    *reinterpret_cast<uint4*>(sV + blk * C::kVPage + (D + row) * 32 + half * 16) =
-        make_uint4(one, one, one, one);
-  }
-  fence_proxy_async_smem();
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -296,31 +381,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4 || warp == 6) {
+  if (warp == 8 || warp == 10) {
     if (n_units > 0) {
-      // -------- TMA producers: warp 4 loads Q and K, warp 6 loads V --------
-      // lane p < 8 issues page p of a unit; page ids are fetched one unit ahead
-      const bool is_k = warp == 4;
+      // -------- TMA producers: warp 8 loads Q and K, warp 10 loads V --------
+      const bool is_k = warp == 8;
       if (is_k && lane == 0) {
         prefetch_tensormap(&tmQ);
-        prefetch_tensormap(&tmK);
-        mbar_expect_tx(q_full, (uint32_t)C::kQ);
-        for (int slab = 0; slab < D / 64; ++slab)
-          tma_load_3d(sQ + slab * C::kSlab, &tmQ, q_full, slab * 64, hkv * a.G,
-                      (int32_t)(sd.node_start + td.t0));
+        prefetch_tensormap(&tmKr);
+        prefetch_tensormap(&tmK1);
+        mbar_expect_tx(q_full, (uint32_t)(2 * C::kQHalf));
+        for (int h = 0; h < 2; ++h)
+          for (int slab = 0; slab < D / 64; ++slab)
+            tma_load_3d(sQ + h * C::kQHalf + slab * C::kQSlab, &tmQ, q_full, slab * 64, hkv * G,
+                        (int32_t)(sd.node_start + td.t0 + h * (kHalf / G)));
       }
-      if (!is_k && lane == 0) prefetch_tensormap(&tmV);
+      if (!is_k && lane == 0) {
+        prefetch_tensormap(&tmVr);
+        prefetch_tensormap(&tmV1);
+      }
       const int n_st = is_k ? kKStages : kVStages;
       uint64_t* full = is_k ? k_full : v_full;
       uint64_t* empty = is_k ? k_empty : v_empty;
-      const uint32_t bytes = is_k ? (uint32_t)C::kK : (uint32_t)(kPages * D * 32);
-      Cursor cur = cursor_at(a, sd, td);
-      auto page_of = [&](const Cursor& c) -> int {
+      const uint32_t bytes = is_k ? (uint32_t)C::kK : (uint32_t)C::kV;
+      UnitWalk walk;
+      walk.start(a, sd, td);
+      int page = 0;
+      bool in_seg = false;
+      auto fetch_page = [&](const Cursor& c) {
         int pi = c.j * kPages + lane;
-        if (pi >= c.n_pages) pi = c.n_pages - 1;  // finite filler; its keys are masked
-        return a.page_ids[c.page_off + pi];
+        in_seg = pi < c.n_pages;
+        if (!in_seg) pi = c.n_pages - 1;  // finite filler; its keys are masked
+        page = a.page_ids[c.page_off + pi];
       };
-      int page = lane < kPages ? page_of(cur) : 0;
+      if (lane < kPages) fetch_page(walk.cur);
       int s = 0;
       uint32_t ph = 0;
       int issued[kKStages > kVStages ? kKStages : kVStages];
@@ -333,23 +426,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
+        const int p0 = __shfl_sync(0xffffffffu, page, 0);
+        const bool run = __all_sync(0xffffffffu, lane >= kPages || (in_seg && page == p0 + lane));
         if (lane == 0) mbar_expect_tx(&full[s], bytes);
         __syncwarp();
-        if (lane < kPages) {
-          if (is_k) {
-            unsigned char* dK = sK + s * C::kK;
-            const int kb = (page * 2 + 0) * a.Hkv + hkv;
+        unsigned char* dst = is_k ? sK + s * C::kK : sV + s * C::kV;
+        if (run) {
+          if (lane == 0)
             for (int slab = 0; slab < D / 64; ++slab)
-              tma_load_2d_nohint(dK + slab * C::kSlab + lane * (kPageSize * 128), &tmK, &full[s],
-                                 slab * 64, kb * kPageSize);
-          } else {
-            const int vb = (page * 2 + 1) * a.Hkv + hkv;
-            tma_load_2d_nohint(sV + s * C::kV + lane * C::kVPage, &tmV, &full[s], 0, vb * D);
-          }
+              tma_load_4d(dst + slab * C::kKSlab, is_k ? &tmKr : &tmVr, &full[s], slab * 64, 0, hkv, p0);
+        } else if (lane < kPages) {
+          for (int slab = 0; slab < D / 64; ++slab)
+            tma_load_4d(dst + slab * C::kKSlab + lane * (kPageSize * 128), is_k ? &tmK1 : &tmV1,
+                        &full[s], slab * 64, 0, hkv, page);
         }
         issued[s] = (int)ph;
-        cursor_next(cur, a, sd, td);
-        if (it + 1 < n_units && lane < kPages) page = page_of(cur);
+        walk.next(a, sd, td);
+        if (it + 1 < n_units && lane < kPages) fetch_page(walk.cur);
         if (++s == n_st) {
           s = 0;
           ph ^= 1;
@@ -363,108 +456,117 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (issued[i] >= 0) mbar_wait(&full[i], (uint32_t)issued[i], nullptr);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     if (lane == 0 && n_units > 0) {
       // ---------------- MMA issuer ----------------
-      const uint32_t idesc_qk = umma_idesc_bf16_f32(kRowsPerTile, kKeysPerUnit);
-      const uint32_t idesc_pv = umma_idesc_bf16_f32(kRowsPerTile, C::kVRows);
+      // Per unit j, in tensor-pipe order: PV_A(j-1), QK_A(j), PV_B(j-1), QK_B(j).
+      // QK_h(j) overwrites S_h, where P_h(j-1) lives, only after PV_h(j-1)
+      // (in-order pipe); the commit after QK_h(j) therefore also tells the
+      // softmax that PV_h(j-1) is done and O_h may be rescaled.
+      const uint32_t idesc_qk = umma_idesc_bf16_f32(kHalf, kKeysPerUnit);
+      const uint32_t idesc_pv = umma_idesc_bf16_f32(kHalf, D) | (1u << 16);  // B (V) MN-major
       const uint32_t q_addr = smem_u32(sQ);
-      const uint32_t p_addr = smem_u32(sP);
+      const int n_halves = has_b ? 2 : 1;
       bool ok = mbar_wait(q_full, 0, abort_flag);
       int ks = 0, vs = 0;
       uint32_t kph = 0, vph = 0;
-      auto issue_pv = [&](int j) -> bool {
-        if (!mbar_wait(p_full, (uint32_t)(j & 1), abort_flag)) return false;
-        if (!mbar_wait(&v_full[vs], vph, abort_flag)) return false;
+      auto pv = [&](int h, int j) -> bool {
+        if (!mbar_wait(&p_full[h], (uint32_t)(j & 1), abort_flag)) return false;
+        if (h == 0 && !mbar_wait(&v_full[vs], vph, abort_flag)) return false;
         tc_fence_after();
         const uint32_t v_addr = smem_u32(sV + vs * C::kV);
+        const uint32_t p_col = tmem + C::kColS + (uint32_t)(h * kKeysPerUnit);
+        const uint32_t o_col = tmem + C::kColO + (uint32_t)(h * D);
 #pragma unroll
-        for (int p = 0; p < kPages; ++p) {
-          const uint64_t da = umma_desc_k_sw128(p_addr + (p >> 2) * C::kSlab + (p & 3) * 32);
-          const uint64_t db = umma_desc_k_sw32(v_addr + p * C::kVPage);
-          umma_bf16(tmem + C::kColO, da, db, idesc_pv, (j > 0 || p > 0) ? 1u : 0u);
-        }
-        umma_commit(&v_empty[vs]);
-        umma_commit(pv_done);
-        if (++vs == kVStages) {
-          vs = 0;
-          vph ^= 1;
+        for (int p = 0; p < kPages; ++p)
+          umma_bf16_tmem_a(o_col, p_col + 8 * p,
+                           umma_desc_mn_sw128(v_addr + p * (kPageSize * 128), C::kKSlab), idesc_pv,
+                           (j > 0 || p > 0) ? 1u : 0u);
+        if (h == n_halves - 1) {
+          umma_commit(&v_empty[vs]);
+          if (++vs == kVStages) {
+            vs = 0;
+            vph ^= 1;
+          }
         }
         return true;
       };
       for (int it = 0; it < n_units && ok; ++it) {
-        const int sb = it & 1;
-        if (!mbar_wait(&k_full[ks], kph, abort_flag) ||
-            !mbar_wait(&s_empty[sb], (uint32_t)(((it >> 1) & 1) ^ 1), abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t k_addr = smem_u32(sK + ks * C::kK);
+        for (int h = 0; h < n_halves; ++h) {
+          if (it > 0 && !pv(h, it - 1)) {
+            ok = false;
+            break;
+          }
+          if (h == 0 && !mbar_wait(&k_full[ks], kph, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t k_addr = smem_u32(sK + ks * C::kK);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kSlab + (kk & 3) * 32;
-          umma_bf16(tmem + (uint32_t)(sb * kKeysPerUnit), umma_desc_k_sw128(q_addr + off),
-                    umma_desc_k_sw128(k_addr + off), idesc_qk, kk > 0 ? 1u : 0u);
-        }
-        umma_commit(&k_empty[ks]);
-        umma_commit(&s_full[sb]);
-        if (++ks == kKStages) {
-          ks = 0;
-          kph ^= 1;
-        }
-        if (it > 0 && !issue_pv(it - 1)) {
-          ok = false;
-          break;
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t qo = h * C::kQHalf + (kk >> 2) * C::kQSlab + (kk & 3) * 32;
+            const uint32_t ko = (kk >> 2) * C::kKSlab + (kk & 3) * 32;
+            umma_bf16(tmem + C::kColS + (uint32_t)(h * kKeysPerUnit), umma_desc_k_sw128(q_addr + qo),
+                      umma_desc_k_sw128(k_addr + ko), idesc_qk, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(&s_full[h]);
+          if (h == n_halves - 1) {
+            umma_commit(&k_empty[ks]);
+            if (++ks == kKStages) {
+              ks = 0;
+              kph ^= 1;
+            }
+          }
         }
       }
-      if (ok) ok = issue_pv(n_units - 1);
+      for (int h = 0; h < n_halves && ok; ++h) ok = pv(h, n_units - 1);
       if (!ok) {
         if (!*abort_flag) raise_error(a.err, kErrTimeout);
         *abort_flag = 1;
       }
-      umma_commit(drain);
-      mbar_wait(drain, 0, nullptr);
+      umma_commit(o_full);  // every product issued so far, also on the abort path
+      mbar_wait(o_full, 0, nullptr);
     }
-  } else if (warp < 4 && n_units > 0) {
-    // ---------------- softmax / epilogue (warps 0..3) ----------------
-    const int r = threadIdx.x;  // query row = TMEM lane
-    const int G = a.G;
-    const int tok = r / G;
-    const int token = td.t0 + tok;  // position within the own segment
-    const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);
+  } else if (warp < 8 && n_units > 0 && (warp < 4 || has_b)) {
+    // ---------------- softmax / epilogue of one half ----------------
+    const int h = warp >> 2;
+    const int r = threadIdx.x & 127;  // row within the half = TMEM lane
+    const int tok = h * (kHalf / G) + r / G;
+    const int token = td.t0 + tok;    // position within the own segment
+    const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    const uint32_t s_col = C::kColS + (uint32_t)(h * kKeysPerUnit);
+    const uint32_t o_col = C::kColO + (uint32_t)(h * D);
     const float scale = a.scale_log2;
     float m_used = -INFINITY;  // running max, in scaled log2 units
-    Cursor cur = cursor_at(a, sd, td);
+    float l = 0.f;             // running sum of exp2(s * scale - m_used)
+    UnitWalk walk;
+    walk.start(a, sd, td);
     bool ok = true;
     for (int it = 0; it < n_units; ++it) {
-      const int sb = it & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[sb], (uint32_t)((it >> 1) & 1), abort_flag))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[h], (uint32_t)(it & 1), abort_flag))) {
         ok = false;
         break;
       }
       tc_fence_after();
       float sv[kKeysPerUnit];
-#pragma unroll
-      for (int c = 0; c < kKeysPerUnit / 32; ++c) {
-        float t[32];
-        tmem_ld32(trow + (uint32_t)(sb * kKeysPerUnit + 32 * c), t);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) sv[32 * c + i] = t[i];
-      }
-      tc_fence_before();
-      mbar_arrive(&s_empty[sb]);
+      tmem_ld128(trow + s_col, sv);
       // visible keys of this row in this unit: c < lim
-      const int key0 = cur.j * kKeysPerUnit;
-      int lim = cur.len - key0;
-      if (cur.own) lim = min(lim, token - key0 + 1);
+      const int key0 = walk.cur.j * kKeysPerUnit;
+      int lim = walk.cur.len - key0;
+      if (walk.cur.own) lim = min(lim, token - key0 + 1);
       if (__any_sync(0xffffffffu, lim < kKeysPerUnit)) {
 #pragma unroll
         for (int c = 0; c < kKeysPerUnit; ++c) sv[c] = c < lim ? sv[c] : -INFINITY;
       }
-      float mt = sv[0];
+      // tree maximum: eight independent chains of three-input maxima
+      float mx8[8];
 #pragma unroll
-      for (int c = 1; c < kKeysPerUnit; ++c) mt = fmaxf(mt, sv[c]);
+      for (int c = 0; c < 8; ++c) mx8[c] = fmaxf(sv[2 * c], sv[2 * c + 1]);
+#pragma unroll
+      for (int c = 16; c < kKeysPerUnit; c += 2) mx8[(c >> 1) & 7] = max3(mx8[(c >> 1) & 7], sv[c], sv[c + 1]);
+      const float mt = fmaxf(max3(mx8[0], mx8[1], mx8[2]), fmaxf(max3(mx8[3], mx8[4], mx8[5]),
+                                                                 fmaxf(mx8[6], mx8[7])));
       const float m_new = fmaxf(m_used, mt * scale);
       float alpha = 1.f;
       if (m_new > m_used + kRescaleLog2) {  // also true for the first finite max
@@ -472,59 +574,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_used = m_new;
       }
       const float nbase = m_used == -INFINITY ? 0.f : -m_used;
+      const uint64_t sc2 = f2(scale, scale), nb2 = f2(nbase, nbase);
+      uint32_t pw[kKeysPerUnit / 2];
+      uint64_t sum4[4] = {0, 0, 0, 0};
 #pragma unroll
-      for (int c = 0; c < kKeysPerUnit; ++c) sv[c] = ex2(fmaf(sv[c], scale, nbase));
-      if (it > 0 &&
-          !__all_sync(0xffffffffu, mbar_wait(pv_done, (uint32_t)((it - 1) & 1), abort_flag))) {
-        ok = false;
-        break;
+      for (int c = 0; c < kKeysPerUnit; c += 2) {
+        float x0, x1;
+        uf2(fma_f2(f2(sv[c], sv[c + 1]), sc2, nb2), x0, x1);
+        const float p0 = ex2(x0), p1 = ex2(x1);
+        sum4[(c >> 1) & 3] = add_f2(sum4[(c >> 1) & 3], f2(p0, p1));
+        pw[c >> 1] = pack_bf16(p0, p1);
       }
-      tc_fence_after();
+      float s0, s1, s2, s3, s4, s5, s6, s7;
+      uf2(sum4[0], s0, s1);
+      uf2(sum4[1], s2, s3);
+      uf2(sum4[2], s4, s5);
+      uf2(sum4[3], s6, s7);
+      l = l * alpha + (((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7)));
+      // O_h is stable: PV_h of the previous unit completed before S_h arrived
       if (it > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           float o[32];
-          tmem_ld32(trow + C::kColO + 32 * c, o);
+          tmem_ld32(trow + o_col + 32 * c, o);
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] *= alpha;
-          tmem_st32(trow + C::kColO + 32 * c, o);
+          tmem_st32(trow + o_col + 32 * c, o);
         }
-        tmem_st1_sync(trow + C::kColSum, tmem_ld1_sync(trow + C::kColSum) * alpha);
       }
-      // P row -> shared memory, bf16, 128B swizzle (2 slabs of 64 keys)
-      unsigned char* prow = sP + (r >> 3) * 1024 + (r & 7) * 128;
-#pragma unroll
-      for (int ch = 0; ch < kKeysPerUnit / 8; ++ch) {
-        uint4 w;
-        w.x = pack_bf16(sv[8 * ch + 0], sv[8 * ch + 1]);
-        w.y = pack_bf16(sv[8 * ch + 2], sv[8 * ch + 3]);
-        w.z = pack_bf16(sv[8 * ch + 4], sv[8 * ch + 5]);
-        w.w = pack_bf16(sv[8 * ch + 6], sv[8 * ch + 7]);
-        const int slab = ch >> 3, cc = ch & 7;
-        *reinterpret_cast<uint4*>(prow + slab * C::kSlab + ((cc ^ (r & 7)) << 4)) = w;
-      }
-      fence_proxy_async_smem();
+      // P_h (bf16 pairs) over the first 64 columns of S_h
+      tmem_st64(trow + s_col, pw);
       tc_fence_before();
-      mbar_arrive(p_full);
-      cursor_next(cur, a, sd, td);
+      mbar_arrive(&p_full[h]);
+      walk.next(a, sd, td);
     }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(pv_done, (uint32_t)((n_units - 1) & 1), abort_flag));
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_full, 0, abort_flag));
     if (!ok) {
       if (!*abort_flag) raise_error(a.err, kErrTimeout);
       *abort_flag = 1;
     } else {
       tc_fence_after();
-      const float l = tmem_ld1_sync(trow + C::kColSum);
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const float lse = l > 0.f ? (m_used + __log2f(l)) * 0.69314718055994531f : -INFINITY;
       const bool row_ok = tok < td.nt;
       const int head = hkv * G + (r % G);
       const size_t orow = (size_t)(sd.node_start + token) * a.Hq + head;
-      const size_t prow_i = ((size_t)td.part * a.Hkv + hkv) * kRowsPerTile + r;
+      const size_t prow_i = ((size_t)td.part * a.Hkv + hkv) * kRowsPerTile + h * kHalf + r;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         float o[32];
-        tmem_ld32(trow + C::kColO + 32 * c, o);
+        tmem_ld32(trow + o_col + 32 * c, o);
         if (!row_ok) continue;
         if (td.part < 0) {
           uint4* dst = reinterpret_cast<uint4*>(a.out + orow * D + 32 * c);
@@ -555,14 +654,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
 }
 
 // Combine the partial (O, lse) of split tiles: O = sum_i e^(lse_i - L) O_i,
-// L = ln sum_i e^(lse_i).  One warp per query row (grid.x = merges x 16
+// L = ln sum_i e^(lse_i).  One warp per query row (grid.x = merges x 32
 // blocks of 8 rows, grid.y = KV head), lanes across head_dim; the loads of
 // every part are in flight together.
 template <int D>
@@ -572,9 +671,9 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const SegDesc* segs, co
                                                          int G) {
   constexpr int PER = D / 32;
   constexpr int kBatch = 8;
-  const MergeDesc md = merges[blockIdx.x >> 4];
+  const MergeDesc md = merges[blockIdx.x >> 5];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = (blockIdx.x & 15) * 8 + warp;
+  const int row = (blockIdx.x & 31) * 8 + warp;
   const int hkv = blockIdx.y;
   if (row / G >= md.nt) return;
   const size_t step = (size_t)Hkv * kRowsPerTile;
@@ -625,14 +724,13 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const SegDesc* segs, co
 }
 
 // Copy the K/V of one 16-token page of a segment, for one KV head (grid.y),
-// into its pool page.  Pool page layout: K as [Hkv][16][D], V transposed as
-// [Hkv][D][16]; slots past the segment end are zero-filled.
+// into its pool page.  Pool page layout: K as [Hkv][16][D], then V as
+// [Hkv][16][D]; slots past the segment end are zero-filled.
 template <int D>
 __global__ void __launch_bounds__(256) kv_append_kernel(const SegDesc* segs, const int32_t* page_ids,
                                                         const AppendDesc* app, const bf16* k,
                                                         const bf16* v, bf16* pool, int Hkv) {
   constexpr int CPR = D / 8;
-  __shared__ __align__(16) bf16 sv[kPageSize][D + 8];
   const AppendDesc ad = app[blockIdx.x];
   const int h = blockIdx.y;
   const SegDesc sd = segs[ad.seg];
@@ -640,7 +738,7 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const SegDesc* segs, con
   const int ntok = min(kPageSize, sd.len - tok0);
   const int page = page_ids[sd.page_off + ad.page_in_seg];
   const size_t kbase = (((size_t)page * 2) * Hkv + h) * kPageSize * D;
-  const size_t vbase = (((size_t)page * 2 + 1) * Hkv + h) * (size_t)D * kPageSize;
+  const size_t vbase = (((size_t)page * 2 + 1) * Hkv + h) * kPageSize * D;
   for (int i = threadIdx.x; i < kPageSize * CPR; i += blockDim.x) {
     const int ch = i % CPR, slot = i / CPR;
     uint4 kk = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
@@ -650,16 +748,7 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const SegDesc* segs, con
       vv = *reinterpret_cast<const uint4*>(v + src);
     }
     *reinterpret_cast<uint4*>(pool + kbase + (size_t)slot * D + ch * 8) = kk;
-    *reinterpret_cast<uint4*>(&sv[slot][ch * 8]) = vv;
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < D * 2; i += blockDim.x) {
-    const int dd = i >> 1, half = i & 1;
-    uint4 w;
-    bf16* e = reinterpret_cast<bf16*>(&w);
-#pragma unroll
-    for (int t = 0; t < 8; ++t) e[t] = sv[half * 8 + t][dd];
-    *reinterpret_cast<uint4*>(pool + vbase + (size_t)dd * kPageSize + half * 8) = w;
+    *reinterpret_cast<uint4*>(pool + vbase + (size_t)slot * D + ch * 8) = vv;
   }
 }
 
@@ -667,7 +756,7 @@ bool encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims
             const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swz) {
   EncodeTiledFn enc = get_encode_tiled();
   if (!enc) return false;
-  cuuint32_t estr[3] = {1, 1, 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), dims,
              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -696,27 +785,35 @@ cudaError_t run_call(const AttnLaunch& L) {
   float* part_o = static_cast<float*>(L.workspace);
   float* part_lse = part_o + (size_t)L.n_parts * L.Hkv * kRowsPerTile * D;
   if (L.n_tiles > 0) {
-    CUtensorMap tmQ, tmK, tmV;
+    CUtensorMap tmQ, tmKr, tmK1, tmVr, tmV1;
     {
       cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)L.Hq, (cuuint64_t)L.node_tokens};
       cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)L.Hq * D * 2};
-      cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)(kRowsPerTile / G)};
+      cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)(kHalf / G)};
       if (!encode(&tmQ, L.q, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     }
-    const cuuint64_t blocks = (cuuint64_t)L.pool_pages * 2 * L.Hkv;
+    // pool page: [K: Hkv][16][D] then [V: Hkv][16][D]; dims (inner first)
+    const cuuint64_t page_bytes = (cuuint64_t)2 * L.Hkv * kPageSize * D * 2;
     {
-      cuuint64_t dims[2] = {(cuuint64_t)D, blocks * kPageSize};
-      cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-      cuuint32_t box[2] = {64, (cuuint32_t)kPageSize};
-      if (!encode(&tmK, pool, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)kPageSize, (cuuint64_t)L.Hkv,
+                            (cuuint64_t)L.pool_pages};
+      cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)kPageSize * D * 2, page_bytes};
+      cuuint32_t boxr[4] = {64, (cuuint32_t)kPageSize, 1, (cuuint32_t)kPages};
+      cuuint32_t box1[4] = {64, (cuuint32_t)kPageSize, 1, 1};
+      if (!encode(&tmKr, pool, 4, dims, strides, boxr, CU_TENSOR_MAP_SWIZZLE_128B) ||
+          !encode(&tmK1, pool, 4, dims, strides, box1, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     }
     {
-      cuuint64_t dims[2] = {(cuuint64_t)kPageSize, blocks * D};
-      cuuint64_t strides[1] = {(cuuint64_t)kPageSize * 2};
-      cuuint32_t box[2] = {(cuuint32_t)kPageSize, (cuuint32_t)D};
-      if (!encode(&tmV, pool, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_32B))
+      const bf16* vbase = pool + (size_t)L.Hkv * kPageSize * D;
+      cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)kPageSize, (cuuint64_t)L.Hkv,
+                            (cuuint64_t)L.pool_pages};
+      cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)kPageSize * D * 2, page_bytes};
+      cuuint32_t boxr[4] = {64, (cuuint32_t)kPageSize, 1, (cuuint32_t)kPages};
+      cuuint32_t box1[4] = {64, (cuuint32_t)kPageSize, 1, 1};
+      if (!encode(&tmVr, vbase, 4, dims, strides, boxr, CU_TENSOR_MAP_SWIZZLE_128B) ||
+          !encode(&tmV1, vbase, 4, dims, strides, box1, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     }
     AttnArgs a;
@@ -738,11 +835,11 @@ cudaError_t run_call(const AttnLaunch& L) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)L.n_tiles, (unsigned)L.Hkv);
-    attn_tc_kernel<D><<<grid, kThreads, smem, st>>>(tmQ, tmK, tmV, a);
+    attn_tc_kernel<D><<<grid, kThreads, smem, st>>>(tmQ, tmKr, tmK1, tmVr, tmV1, a);
     ++launches;
   }
   if (L.n_merges > 0) {
-    dim3 grid((unsigned)L.n_merges * 16, (unsigned)L.Hkv);
+    dim3 grid((unsigned)L.n_merges * 32, (unsigned)L.Hkv);
     attn_merge_kernel<D><<<grid, 256, 0, st>>>(segs, merges, part_o, part_lse,
                                                static_cast<bf16*>(L.out), L.lse, L.Hq, L.Hkv, G);
     ++launches;

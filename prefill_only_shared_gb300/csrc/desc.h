@@ -5,8 +5,8 @@
 
 namespace sp {
 
-constexpr int kRowsPerTile = 128;  // query rows (token x group-head) per CTA tile
-constexpr int kKeysPerUnit = 128;  // keys per KV unit (8 pages of 16): one MMA N tile
+constexpr int kRowsPerTile = 256;  // query rows (token x group-head) per CTA tile: two 128-row halves
+constexpr int kKeysPerUnit = 128;  // keys per KV unit (8 pages of 16): one N=128 MMA
 constexpr int kPageSize = 16;      // tokens per KV page
 
 // One trie segment.  Its K/V live in pages page_ids[page_off ..]; its

@@ -41,7 +41,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 bool shape_ok(const sp_shape& s) {
   if (s.n_q_heads <= 0 || s.n_kv_heads <= 0 || s.n_q_heads % s.n_kv_heads) return false;
   int g = s.n_q_heads / s.n_kv_heads;
-  if (g > sp::kRowsPerTile || sp::kRowsPerTile % g) return false;
+  if (g > 128 || 128 % g) return false;  // each 128-row half holds whole tokens
   if (s.head_dim != 64 && s.head_dim != 128) return false;
   if (s.page_size != sp::kPageSize) return false;
   if (s.hidden <= 0 || s.hidden % 8) return false;
@@ -336,10 +336,24 @@ extern "C" sp_status sp_plan_build(const sp_shape* shape, int32_t n_branches,
         }
       }
       call.n_append = (int64_t)appends.size() - call.append_off;
-      // split long tiles so the call fills the GPU, then longest first
-      int64_t total_units = 0;
-      for (auto& x : raw) total_units += x.units;
-      int64_t budget = std::max<int64_t>(kMinUnitsPerPart, ceil_div(std::max<int64_t>(total_units, 1), part_target));
+      // When the call has fewer tiles than one wave of CTAs, split the long
+      // tiles' KV walks into parts (merged afterwards) so the call fills the
+      // GPU, keeping the total within one wave; then schedule longest first.
+      int64_t total_units = 0, max_units = 0;
+      for (auto& x : raw) {
+        total_units += x.units;
+        max_units = std::max<int64_t>(max_units, x.units);
+      }
+      int64_t budget = std::max<int64_t>(max_units, 1);  // no split
+      if ((int64_t)raw.size() < part_target) {
+        budget = std::max<int64_t>(kMinUnitsPerPart, ceil_div(std::max<int64_t>(total_units, 1), part_target));
+        auto n_ctas = [&](int64_t b) {
+          int64_t n = 0;
+          for (auto& x : raw) n += ceil_div(x.units, b);
+          return n;
+        };
+        while (budget < max_units && n_ctas(budget) > part_target) ++budget;
+      }
       struct Work { sp::TileDesc t; int64_t units; };
       std::vector<Work> work;
       call.merge_off = (int64_t)merges.size();

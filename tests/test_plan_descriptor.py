@@ -23,7 +23,7 @@ TILE = np.dtype([("seg", "<i4"), ("t0", "<i4"), ("nt", "<i4"), ("u_lo", "<i4"), 
 MERGE = np.dtype([("seg", "<i4"), ("t0", "<i4"), ("nt", "<i4"), ("part0", "<i4"), ("nparts", "<i4"),
                   ("p0", "<i4"), ("p1", "<i4"), ("p2", "<i4")])
 APP = np.dtype([("seg", "<i4"), ("page", "<i4")])
-ROWS, UNIT, PAGE = 128, 128, 16
+ROWS, UNIT, PAGE = 256, 128, 16
 
 
 def decode(blob):
