@@ -117,17 +117,22 @@ def load_peaks():
 
 
 def kernel_traffic(kernel_file: str, config: str):
-    """dram bytes per launch from the committed ncu summary, if the kernel
-    source is unchanged since it was captured; else None."""
+    """DRAM bytes per launch from the committed ncu summary
+    (profiles/traffic_<kernel>_<config>.txt), if the kernel source is unchanged
+    since it was captured; else None."""
     src = os.path.join(ROOT, "prefill_only_shared_gb300", "csrc", kernel_file)
-    summ = os.path.join(ROOT, "profiles", f"traffic_{os.path.splitext(kernel_file)[0]}_{config}.json")
+    summ = os.path.join(ROOT, "profiles", f"traffic_{os.path.splitext(kernel_file)[0]}_{config}.txt")
     if not (os.path.exists(src) and os.path.exists(summ)):
         return None
-    d = json.load(open(summ))
+    fields = {}
+    for line in open(summ):
+        if ":" in line and not line.startswith(("#", "|", " ")):
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip()
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
-    if d.get("source_sha256") != sha:
+    if fields.get("source_sha256") != sha or "dram_bytes_per_launch" not in fields:
         return None
-    return d.get("dram_bytes_per_launch")
+    return int(fields["dram_bytes_per_launch"])
 
 
 # --------------------------------------------------------------------------
@@ -337,7 +342,7 @@ def run_libsp(args, ws, rank, local):
                      "label_softmax": round(statistics.mean(sm_ms), 5),
                      "plan_and_launch_overhead": round(ms - attn_avg - lm_avg - statistics.mean(sm_ms), 5)},
         "roofline": {
-            "kernel": "lmhead_kernel (sp_label_logprobs: streaming kernel + its finalize launch)",
+            "kernel": "lmhead_kernel (the whole sp_label_logprobs call: barrier-counter memset + one cooperative launch)",
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peaks["hbm_gbs"],

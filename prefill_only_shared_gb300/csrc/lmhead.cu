@@ -14,8 +14,9 @@
 //               thread), per-column max / sum-of-exp over the 128 rows, merged
 //               into a running (max, sum) per branch; label logits picked out
 //               of TMEM when a label id falls in the tile.
-// A finalize kernel merges the per-CTA (max, sum) pairs into lse and turns
-// the label logits into log-probabilities.
+// After a grid barrier (cooperative launch, one CTA per SM), every warp of
+// the grid merges the per-CTA (max, sum) pairs of some branches into lse and
+// turns their label logits into log-probabilities.
 #include <mutex>
 
 #include "common.cuh"
@@ -40,8 +41,10 @@ struct LmArgs {
   uint32_t tmem_cols;
   const int32_t* label_off;
   const int32_t* label_ids;
-  float* logits_out;  // raw label logits, [n_labels]
+  float* logits_out;  // raw label logits, [n_labels]; log-probabilities on exit
+  float* lse;         // [N]
   float2* partials;   // [gridDim.x][N]
+  unsigned* grid_arrivals;  // zero at launch
   unsigned* err;
 };
 
@@ -255,39 +258,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, a.tmem_cols);
   }
-}
 
-// One warp per branch: merge the per-CTA partials into lse and convert the
-// raw label logits into log-probabilities.
-__global__ void __launch_bounds__(128) lmhead_finalize_kernel(const float2* partials, int n_parts,
-                                                              int N, int V,
-                                                              const int32_t* label_off,
-                                                              const int32_t* label_ids,
-                                                              float* logprobs, float* lse,
-                                                              unsigned* err) {
-  const int n = blockIdx.x * 4 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (n >= N) return;
-  float m = -INFINITY, s = 0.f;
-  for (int p = lane; p < n_parts; p += 32) {
-    const float2 v = partials[(size_t)p * N + n];
-    lse_merge(m, s, v.x, v.y);
+  // ---- grid barrier (the launch is cooperative: every CTA is resident) ----
+  volatile int* go = abort_flag;  // reused as the barrier verdict
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(a.grid_arrivals, 1u);
+    const unsigned long long t0 = globaltimer();
+    int ok = 1;
+    while (atomicAdd(a.grid_arrivals, 0u) < gridDim.x) {
+      if (globaltimer() - t0 > kWaitLimitNs) {
+        raise_error(a.err, kErrTimeout);
+        ok = 0;
+        break;
+      }
+    }
+    __threadfence();
+    *go = ok && !*abort_flag;
   }
+  __syncthreads();
+  if (!*go) return;
+
+  // ---- finalize, one warp per branch across the grid: merge the per-CTA
+  // (max, sum) pairs into lse and turn the label logits into log-probs ----
+  const int n_warps = kThreads / 32;
+  for (int n = blockIdx.x * n_warps + warp; n < a.N; n += gridDim.x * n_warps) {
+    float m = -INFINITY, sum = 0.f;
+    for (int p = lane; p < (int)gridDim.x; p += 32) {
+      const float2 v = __ldcg(&a.partials[(size_t)p * a.N + n]);
+      lse_merge(m, sum, v.x, v.y);
+    }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-    lse_merge(m, s, m2, s2);
-  }
-  const float L = m + __logf(s);
-  if (lane == 0) lse[n] = L;
-  for (int j = label_off[n] + lane; j < label_off[n + 1]; j += 32) {
-    const int id = label_ids[j];
-    if (id < 0 || id >= V) {
-      logprobs[j] = __int_as_float(0x7fc00000);
-      raise_error(err, kErrBounds);
-    } else {
-      logprobs[j] = logprobs[j] - L;
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+      const float s2 = __shfl_xor_sync(0xffffffffu, sum, o);
+      lse_merge(m, sum, m2, s2);
+    }
+    const float L = m + __logf(sum);
+    if (lane == 0) a.lse[n] = L;
+    for (int j = a.label_off[n] + lane; j < a.label_off[n + 1]; j += 32) {
+      const int id = a.label_ids[j];
+      if (id < 0 || id >= a.V) {
+        a.logits_out[j] = __int_as_float(0x7fc00000);
+        raise_error(a.err, kErrBounds);
+      } else {
+        a.logits_out[j] = __ldcg(&a.logits_out[j]) - L;
+      }
     }
   }
 }
@@ -334,9 +350,10 @@ bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t oute
 
 }  // namespace
 
+// Workspace: per-CTA partials [grid][N] float2, then the grid-barrier counter.
 size_t lmhead_workspace_bytes(int N, int V, int n_sms) {
   Geometry g = geometry(N, V, n_sms > 0 ? n_sms : 152);
-  return ((size_t)g.grid * N * sizeof(float2) + 255) & ~size_t(255);
+  return ((size_t)g.grid * N * sizeof(float2) + 16 + 255) & ~size_t(255);
 }
 
 cudaError_t lmhead_run(const LmheadLaunch& L) {
@@ -359,28 +376,35 @@ cudaError_t lmhead_run(const LmheadLaunch& L) {
   a.label_ids = L.label_ids;
   a.logits_out = L.logprobs;
   a.partials = static_cast<float2*>(L.workspace);
+  a.grid_arrivals = reinterpret_cast<unsigned*>(a.partials + (size_t)g.grid * L.N);
+  a.lse = L.lse;
   a.err = L.err;
   cudaError_t e = cudaFuncSetAttribute(lmhead_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)g.smem);
   if (e != cudaSuccess) return e;
   cudaStream_t st = static_cast<cudaStream_t>(L.stream);
-  lmhead_kernel<<<g.grid, kThreads, g.smem, st>>>(tmW, tmH, a);
-  lmhead_finalize_kernel<<<(L.N + 3) / 4, 128, 0, st>>>(a.partials, g.grid, L.N, L.V, L.label_off,
-                                                        L.label_ids, L.logprobs, L.lse, L.err);
-  *L.launches = 2;
+  e = cudaMemsetAsync(a.grid_arrivals, 0, sizeof(unsigned), st);
+  if (e != cudaSuccess) return e;
+  void* args[] = {&tmW, &tmH, &a};
+  e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(lmhead_kernel), dim3(g.grid),
+                                  dim3(kThreads), args, g.smem, st);
+  if (e != cudaSuccess) return e;
+  *L.launches = 1;
   return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------
-// No-allocation readout: the per-CTA partials live in this file-scope device
-// array (2 MiB: up to 256 CTAs x 1024 branches x one float2), which every GPU
+// No-allocation readout: the per-CTA partials and the grid-barrier counter
+// live in this file-scope device array (2 MiB + 256 bytes: up to 256 CTAs x
+// 1024 branches x one float2, then the counter), which every GPU
 // that loads the library holds until exit.  Host code cannot use the array's
 // name as a device address, so its address is looked up once per device (with
 // that device current) and passed to the kernel like any workspace.  Calls
 // share the array; each call writes every partial it reads, so nothing needs
 // clearing, and overlapping calls would race.
 namespace {
-constexpr size_t kNoallocScratchBytes = (size_t)kNoallocMaxCtas * kNoallocMaxBranches * sizeof(float2);
+constexpr size_t kNoallocScratchBytes =
+    (size_t)kNoallocMaxCtas * kNoallocMaxBranches * sizeof(float2) + 256;  // + barrier counter
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
 cudaError_t noalloc_scratch_address(void** out) {
