@@ -263,10 +263,79 @@ sp_status sp_label_logprobs_noalloc(const void* h, const void* W, int32_t N, int
 sp_status sp_label_softmax(const float* logprobs, const int32_t* label_off, int32_t N, float* probs,
                            int32_t* argmax, void* stream);
 
+/* Question types (openjev-sglang article, section on the three question
+ * types): a yes/no ("noul") question, a choice among options, and a score
+ * over ordered levels. */
+#define SP_QTYPE_NOUL 0
+#define SP_QTYPE_CHOICE 1
+#define SP_QTYPE_SCORE 2
+
+/* The label softmax of sp_label_softmax fused with the question-type result
+ * and the confidence value, one question per branch whose options are the
+ * branch's labels (openjev-sglang article: request flow step 5, the three
+ * question types, and the confidence section):
+ *
+ *   probs, argmax     exactly as sp_label_softmax
+ *   value[n]          NOUL:   probs of the branch's first label (P(yes))
+ *                     CHOICE: probs of the argmax label (the chosen option's
+ *                             probability; the option itself is argmax[n])
+ *                     SCORE:  sum_i i * probs[i], i = 0 .. k-1
+ *   confidence[n]     1 - H(p) / ln k, H the entropy in nats (0 ln 0 = 0)
+ *
+ *   logprobs   DEVICE fp32 [label_off[N]];  label_off: DEVICE int32 [N+1]
+ *   qtype      DEVICE int32 [N], each SP_QTYPE_*
+ *   probs      DEVICE fp32 [label_off[N]];  argmax: DEVICE int32 [N]
+ *   value, confidence  DEVICE fp32 [N]
+ * Device-side checks: a branch with a label count outside 2..64 gets NaN /
+ * -1 outputs, a qtype outside the three codes a NaN value; both raise
+ * SP_ERR_DEVICE_BOUNDS.  One launch, one warp per branch. */
+sp_status sp_label_decide(const float* logprobs, const int32_t* label_off, const int32_t* qtype,
+                          int32_t N, float* probs, int32_t* argmax, float* value,
+                          float* confidence, void* stream);
+
+/* Questions assembled from yes/no candidate branches (LLM2Jev page: each
+ * choice option and each score level is its own yes/no input, and the final
+ * answers are read after normalisation).  Question q owns the consecutive
+ * branches cand_off[q] .. cand_off[q+1]-1; y_c is candidate branch c's
+ * probability of its first label ("yes"), read from `probs` (the output of
+ * sp_label_softmax or sp_label_decide).
+ *
+ *   CHOICE / SCORE (2..64 candidates):  dist_c = y_c / sum y over the question
+ *       argmax[q] = index within the question of the largest y (lowest on ties)
+ *       value[q]  = dist of the argmax (CHOICE) or sum_i i * dist_i (SCORE)
+ *       confidence[q] = 1 - H(dist) / ln K
+ *   NOUL (exactly 1 candidate):  dist = value = y;  argmax = 0;
+ *       confidence = 1 - H(y, 1 - y) / ln 2
+ *
+ *   probs      DEVICE fp32 [label_off[n_branches]];  label_off: DEVICE int32 [n_branches+1]
+ *   cand_off   DEVICE int32 [n_questions+1], cand_off[0] = 0,
+ *              cand_off[n_questions] <= n_branches
+ *   qtype      DEVICE int32 [n_questions]
+ *   dist       DEVICE fp32 [cand_off[n_questions]];  argmax: DEVICE int32 [n_questions]
+ *   value, confidence  DEVICE fp32 [n_questions]
+ * Device-side checks: a candidate count that does not fit the type, a
+ * qtype outside the three codes, or candidates past n_branches give NaN /
+ * -1 outputs for that question and raise SP_ERR_DEVICE_BOUNDS.  The
+ * normalisation is this library's reading: the page prints no formula. */
+sp_status sp_candidate_decide(const float* probs, const int32_t* label_off, int32_t n_branches,
+                              const int32_t* cand_off, const int32_t* qtype, int32_t n_questions,
+                              float* dist, int32_t* argmax, float* value, float* confidence,
+                              void* stream);
+
 /* Host-side validation of a label CSR (HOST arrays): counts in [2, 64],
  * 0 <= id < vocab, monotone offsets.  SP_OK or SP_ERR_ARG. */
 sp_status sp_check_labels(const int32_t* label_off, const int32_t* label_ids, int32_t N,
                           int32_t vocab);
+
+/* Bounded device wait on a flag, with the time limit and error path of
+ * every pipeline wait inside libsp's kernels: one thread polls *flag until
+ * it equals `expect` or limit_ns of device time (clamped to 1 us .. 2 s) has
+ * passed.  On timeout it raises SP_ERR_DEVICE_TIMEOUT through the device
+ * error word (read by sp_check_device_error) and returns; the context stays
+ * usable.  For checking failure reporting without a fault: a flag that
+ * nothing sets makes the wait run out.
+ *   flag  DEVICE uint32, 4-byte aligned;  limit_ns >= 0 */
+sp_status sp_wait_flag(const uint32_t* flag, uint32_t expect, int64_t limit_ns, void* stream);
 
 /* Synchronise `stream`, read and clear the device error word of the current
  * device.  SP_OK, SP_ERR_DEVICE_TIMEOUT, SP_ERR_DEVICE_BOUNDS or SP_ERR_CUDA. */

@@ -225,6 +225,51 @@ extern "C" sp_status sp_label_softmax(const float* logprobs, const int32_t* labe
   return e == cudaSuccess ? SP_OK : SP_ERR_CUDA;
 }
 
+extern "C" sp_status sp_label_decide(const float* logprobs, const int32_t* label_off,
+                                     const int32_t* qtype, int32_t N, float* probs,
+                                     int32_t* argmax, float* value, float* confidence,
+                                     void* stream) {
+  t_last_launches = 0;
+  if (!logprobs || !label_off || !qtype || !probs || !argmax || !value || !confidence || N < 1)
+    return SP_ERR_ARG;
+  unsigned* err = error_word_ptr();
+  if (!err) return SP_ERR_CUDA;
+  cudaError_t e = sp::label_decide_run(logprobs, label_off, qtype, N, probs, argmax, value,
+                                       confidence, err, stream);
+  t_last_launches = 1;
+  return e == cudaSuccess ? SP_OK : SP_ERR_CUDA;
+}
+
+extern "C" sp_status sp_candidate_decide(const float* probs, const int32_t* label_off,
+                                         int32_t n_branches, const int32_t* cand_off,
+                                         const int32_t* qtype, int32_t n_questions, float* dist,
+                                         int32_t* argmax, float* value, float* confidence,
+                                         void* stream) {
+  t_last_launches = 0;
+  if (!probs || !label_off || !cand_off || !qtype || !dist || !argmax || !value || !confidence ||
+      n_branches < 1 || n_questions < 1)
+    return SP_ERR_ARG;
+  unsigned* err = error_word_ptr();
+  if (!err) return SP_ERR_CUDA;
+  cudaError_t e = sp::candidate_decide_run(probs, label_off, n_branches, cand_off, qtype,
+                                           n_questions, dist, argmax, value, confidence, err,
+                                           stream);
+  t_last_launches = 1;
+  return e == cudaSuccess ? SP_OK : SP_ERR_CUDA;
+}
+
+extern "C" sp_status sp_wait_flag(const uint32_t* flag, uint32_t expect, int64_t limit_ns,
+                                  void* stream) {
+  t_last_launches = 0;
+  if (!flag || (reinterpret_cast<uintptr_t>(flag) & 3u) || limit_ns < 0) return SP_ERR_ARG;
+  unsigned* err = error_word_ptr();
+  if (!err) return SP_ERR_CUDA;
+  cudaError_t e = sp::wait_flag_run(flag, expect, static_cast<unsigned long long>(limit_ns), err,
+                                    stream);
+  t_last_launches = 1;
+  return e == cudaSuccess ? SP_OK : SP_ERR_CUDA;
+}
+
 extern "C" sp_status sp_check_device_error(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SP_ERR_CUDA;
   unsigned word = 0;

@@ -60,6 +60,19 @@ cudaError_t lmhead_run_noalloc(LmheadLaunch L);
 
 cudaError_t label_softmax_run(const float* logprobs, const int32_t* label_off, int N, float* probs,
                               int32_t* argmax, unsigned* err, void* stream);
+cudaError_t label_decide_run(const float* logprobs, const int32_t* label_off, const int32_t* qtype,
+                             int N, float* probs, int32_t* argmax, float* value, float* conf,
+                             unsigned* err, void* stream);
+cudaError_t candidate_decide_run(const float* probs, const int32_t* label_off, int n_branches,
+                                 const int32_t* cand_off, const int32_t* qtype, int Q, float* dist,
+                                 int32_t* argmax, float* value, float* conf, unsigned* err,
+                                 void* stream);
+
+// One thread polls *flag until it equals `expect` or limit_ns (clamped to
+// 1 us .. kWaitLimitNs) passes; on timeout the device error word gets
+// kErrTimeout.
+cudaError_t wait_flag_run(const unsigned* flag, unsigned expect, unsigned long long limit_ns,
+                          unsigned* err, void* stream);
 
 // cuTensorMapEncodeTiled, fetched from the driver through the runtime.
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,

@@ -439,56 +439,4 @@ cudaError_t lmhead_run_noalloc(LmheadLaunch L) {
   return lmhead_run(L);
 }
 
-// ---------------------------------------------------------------------------
-// Label softmax: one warp per branch, <= 64 labels (two per lane).
-__global__ void __launch_bounds__(128) label_softmax_kernel(const float* lp, const int32_t* off,
-                                                            int N, float* probs, int32_t* argmax,
-                                                            unsigned* err) {
-  const int n = blockIdx.x * 4 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (n >= N) return;
-  const int a0 = off[n], k = off[n + 1] - a0;
-  if (k < 2 || k > 64) {
-    for (int j = lane; j < (k > 0 ? k : 0); j += 32) probs[a0 + j] = __int_as_float(0x7fc00000);
-    if (lane == 0) {
-      argmax[n] = -1;
-      raise_error(err, kErrBounds);
-    }
-    return;
-  }
-  const float x0 = lane < k ? lp[a0 + lane] : -INFINITY;
-  const float x1 = lane + 32 < k ? lp[a0 + lane + 32] : -INFINITY;
-  // argmax with the lowest index on ties
-  float bv = x0;
-  int bi = lane;
-  if (x1 > bv) {
-    bv = x1;
-    bi = lane + 32;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-    if (ov > bv || (ov == bv && oi < bi)) {
-      bv = ov;
-      bi = oi;
-    }
-  }
-  const float m = bv;
-  const float e0 = lane < k ? __expf(x0 - m) : 0.f;
-  const float e1 = lane + 32 < k ? __expf(x1 - m) : 0.f;
-  const float s = warp_sum(e0 + e1);
-  const float inv = 1.f / s;
-  if (lane < k) probs[a0 + lane] = e0 * inv;
-  if (lane + 32 < k) probs[a0 + lane + 32] = e1 * inv;
-  if (lane == 0) argmax[n] = bi;
-}
-
-cudaError_t label_softmax_run(const float* logprobs, const int32_t* label_off, int N, float* probs,
-                              int32_t* argmax, unsigned* err, void* stream) {
-  label_softmax_kernel<<<(N + 3) / 4, 128, 0, static_cast<cudaStream_t>(stream)>>>(
-      logprobs, label_off, N, probs, argmax, err);
-  return cudaGetLastError();
-}
-
 }  // namespace sp

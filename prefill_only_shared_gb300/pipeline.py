@@ -26,6 +26,8 @@ class PassOutputs:
     probs: torch.Tensor  # fp32 [n_labels]
     argmax: torch.Tensor  # int32 [N]
     plan: "sp.Plan"
+    value: torch.Tensor | None = None  # fp32 [N], with question types
+    confidence: torch.Tensor | None = None  # fp32 [N], with question types
 
 
 class SharedPrefixClassifier:
@@ -106,20 +108,53 @@ class SharedPrefixClassifier:
         self.last_softmax_launches = sp.sp_last_launch_count()
         return probs, argmax
 
-    def readout(self, h, W, label_off, label_ids, n_labels, stream=None):
+    def decide(self, logprobs, label_off, qtype, stream=None):
+        """One question per branch, its options the branch's labels: label
+        softmax fused with the question type's value and the confidence.
+        Returns (probs, argmax, value, confidence)."""
+        N = label_off.numel() - 1
+        probs = self._buf("probs", logprobs.numel(), torch.float32)
+        argmax = self._buf("argmax", N, torch.int32)
+        value = self._buf("value", N, torch.float32)
+        conf = self._buf("confidence", N, torch.float32)
+        sp.sp_label_decide(logprobs, label_off, qtype, probs, argmax, value, conf, stream)
+        self.last_softmax_launches = sp.sp_last_launch_count()
+        return probs, argmax, value, conf
+
+    def candidates(self, probs, label_off, cand_off, qtype, stream=None):
+        """Questions assembled from yes/no candidate branches (consecutive
+        branches per question).  Returns (dist, argmax, value, confidence)."""
+        Q = cand_off.numel() - 1
+        dist = self._buf("dist", label_off.numel() - 1, torch.float32)  # >= cand_off[-1]
+        argmax = self._buf("q_argmax", Q, torch.int32)
+        value = self._buf("q_value", Q, torch.float32)
+        conf = self._buf("q_confidence", Q, torch.float32)
+        sp.sp_candidate_decide(probs, label_off, cand_off, qtype, dist, argmax, value, conf, stream)
+        self.last_candidate_launches = sp.sp_last_launch_count()
+        return dist, argmax, value, conf
+
+    def readout(self, h, W, label_off, label_ids, n_labels, stream=None, qtype=None):
+        """LM-head label log-probabilities, then the label softmax; with
+        ``qtype`` (device int32 [N]) the softmax is the fused decision and the
+        value / confidence are returned too (else None)."""
         logprobs, lse = self.logprobs(h, W, label_off, label_ids, n_labels, stream)
-        probs, argmax = self.softmax(logprobs, label_off, stream)
+        value = conf = None
+        if qtype is None:
+            probs, argmax = self.softmax(logprobs, label_off, stream)
+        else:
+            probs, argmax, value, conf = self.decide(logprobs, label_off, qtype, stream)
         self.last_readout_launches = self.last_logprob_launches + self.last_softmax_launches
-        return logprobs, lse, probs, argmax
+        return logprobs, lse, probs, argmax, value, conf
 
     def run(self, req_of_branch, tok_offsets, tokens, q, k, v, h, W, label_off, label_ids,
-            stream=None, schedule="rounds") -> PassOutputs:
+            stream=None, schedule="rounds", qtype=None) -> PassOutputs:
         """q/k/v in node-token order of the plan (see sp_plan_segments)."""
         plan = self.plan(req_of_branch, tok_offsets, tokens)
         out, lse = self.attention(plan, q, k, v, stream, schedule)
         n_labels = int(label_ids.numel())
-        logprobs, lse_v, probs, argmax = self.readout(h, W, label_off, label_ids, n_labels, stream)
-        return PassOutputs(out, lse, logprobs, lse_v, probs, argmax, plan)
+        logprobs, lse_v, probs, argmax, value, conf = self.readout(
+            h, W, label_off, label_ids, n_labels, stream, qtype)
+        return PassOutputs(out, lse, logprobs, lse_v, probs, argmax, plan, value, conf)
 
     @property
     def last_launches(self) -> int:

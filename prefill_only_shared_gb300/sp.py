@@ -20,6 +20,7 @@ from . import build as _build
 
 SP_OK = 0
 SP_ALL_ROUNDS = -1
+SP_QTYPE_NOUL, SP_QTYPE_CHOICE, SP_QTYPE_SCORE = 0, 1, 2
 STATUS_NAMES = {0: "SP_OK", 1: "SP_ERR_ARG", 2: "SP_ERR_LIMIT", 3: "SP_ERR_POOL_FULL",
                 4: "SP_ERR_CUDA", 5: "SP_ERR_DEVICE_TIMEOUT", 6: "SP_ERR_DEVICE_BOUNDS",
                 7: "SP_ERR_WORKSPACE"}
@@ -73,6 +74,9 @@ SIGNATURES = {
     "sp_label_logprobs": (_I32, [_P, _P, _I32, _I32, _I32, _P, _P, _I32, _P, _P, _P, _SZ, _P]),
     "sp_label_logprobs_noalloc": (_I32, [_P, _P, _I32, _I32, _I32, _P, _P, _I32, _P, _P, _P]),
     "sp_label_softmax": (_I32, [_P, _P, _I32, _P, _P, _P]),
+    "sp_label_decide": (_I32, [_P, _P, _P, _I32, _P, _P, _P, _P, _P]),
+    "sp_candidate_decide": (_I32, [_P, _P, _I32, _P, _P, _I32, _P, _P, _P, _P, _P]),
+    "sp_wait_flag": (_I32, [_P, ctypes.c_uint32, ctypes.c_int64, _P]),
     "sp_check_labels": (_I32, [_I32P, _I32P, _I32, _I32]),
     "sp_check_device_error": (_I32, [_P]),
     "sp_status_str": (ctypes.c_char_p, [_I32]),
@@ -293,6 +297,39 @@ def sp_label_softmax(logprobs, label_off, probs, argmax, stream=None):
         _dev(logprobs, torch.float32, "logprobs"), _dev(label_off, torch.int32, "label_off"), N,
         _dev(probs, torch.float32, "probs"), _dev(argmax, torch.int32, "argmax"), _stream(stream))
     _check(st, "sp_label_softmax")
+
+
+def sp_label_decide(logprobs, label_off, qtype, probs, argmax, value, confidence, stream=None):
+    N = label_off.numel() - 1
+    if qtype.numel() != N:
+        raise ValueError("qtype must have one entry per branch")
+    st = lib().sp_label_decide(
+        _dev(logprobs, torch.float32, "logprobs"), _dev(label_off, torch.int32, "label_off"),
+        _dev(qtype, torch.int32, "qtype"), N, _dev(probs, torch.float32, "probs"),
+        _dev(argmax, torch.int32, "argmax"), _dev(value, torch.float32, "value"),
+        _dev(confidence, torch.float32, "confidence"), _stream(stream))
+    _check(st, "sp_label_decide")
+
+
+def sp_candidate_decide(probs, label_off, cand_off, qtype, dist, argmax, value, confidence,
+                        stream=None):
+    n_branches = label_off.numel() - 1
+    Q = cand_off.numel() - 1
+    if qtype.numel() != Q:
+        raise ValueError("qtype must have one entry per question")
+    st = lib().sp_candidate_decide(
+        _dev(probs, torch.float32, "probs"), _dev(label_off, torch.int32, "label_off"), n_branches,
+        _dev(cand_off, torch.int32, "cand_off"), _dev(qtype, torch.int32, "qtype"), Q,
+        _dev(dist, torch.float32, "dist"), _dev(argmax, torch.int32, "argmax"),
+        _dev(value, torch.float32, "value"), _dev(confidence, torch.float32, "confidence"),
+        _stream(stream))
+    _check(st, "sp_candidate_decide")
+
+
+def sp_wait_flag(flag, expect: int, limit_ns: int, stream=None):
+    """Bounded device wait until flag[0] == expect (flag: CUDA int32 tensor)."""
+    _check(lib().sp_wait_flag(_dev(flag, torch.int32, "flag"), int(expect) & 0xffffffff,
+                              int(limit_ns), _stream(stream)), "sp_wait_flag")
 
 
 def sp_check_device_error(stream=None):
