@@ -15,7 +15,7 @@
 // are split over several CTAs whose partial (O, lse) are merged by a
 // log-sum-exp combine in a separate, fully parallel kernel.
 //
-// Roles (352 threads, one CTA per SM):
+// Roles (384 threads, one CTA per SM):
 //   warps 0..3 / 4..7  softmax of half A / half B: one query row per thread
 //               (= TMEM lane); S from TMEM, mask, online max with lazy
 //               rescaling (the running max only moves when it grows by more
@@ -27,12 +27,16 @@
 //   warp 10     TMA producer of the V pages (128B swizzle, 2 stages); a unit
 //               whose eight page ids are consecutive comes in one 4-D box per
 //               64-dim slab, otherwise one box per page and slab;
-//   warp 9      MMA issuer, in tensor-pipe order per unit j: PV_A(j-1),
-//               QK_A(j), PV_B(j-1), QK_B(j) with S_h = Q_h K^T (M 128, N 128,
-//               K d, operands in shared memory) and O_h += P_h V (M 128, N d,
-//               K 16 per page, P_h read from TMEM, V an MN-major operand).
-// The two halves alternate on the tensor pipe, so one half's softmax runs
-// while the other half's products do.
+//   warps 9 / 11  MMA issuers of half A / half B, per unit j: PV_h(j-1),
+//               then QK_h(j), with S_h = Q_h K^T (M 128, N 128, K d, operands
+//               in shared memory) and O_h += P_h V (M 128, N d, K 16 per page,
+//               P_h read from TMEM, V an MN-major operand).  A K / V stage is
+//               released when both halves' products that read it are done.
+// The halves take turns on the tensor pipe (A0 B0 A1 B1 ...), so one half's
+// softmax runs while the other half's products do.  Each half has its own
+// issuing thread, which does its barrier waits while the other half's group
+// runs: the pipe holds about one product ahead, so a wait between two issues
+// would leave it idle.
 #include "common.cuh"
 #include "desc.h"
 #include "launch.h"
@@ -42,7 +46,7 @@ namespace {
 
 using bf16 = __nv_bfloat16;
 
-constexpr int kThreads = 352;
+constexpr int kThreads = 384;
 constexpr int kHalf = 128;                        // rows per half tile (MMA M)
 constexpr int kKStages = 3;
 constexpr int kVStages = 2;
@@ -305,7 +309,8 @@ struct UnitWalk {
   int u;
   __device__ __forceinline__ void start(const AttnArgs& a, const SegDesc& sd, const TileDesc& td) {
     const int n = td.u_hi - td.u_lo;
-    u = td.u_lo + (int)((blockIdx.x * 5u + blockIdx.y * 3u) % (unsigned)(n > 0 ? n : 1));
+    const unsigned tile = blockIdx.x / (unsigned)a.Hkv, hkv = blockIdx.x % (unsigned)a.Hkv;
+    u = td.u_lo + (int)((tile * 5u + hkv * 3u) % (unsigned)(n > 0 ? n : 1));
     cur = cursor_at(a, sd, td, u);
   }
   __device__ __forceinline__ void next(const AttnArgs& a, const SegDesc& sd, const TileDesc& td) {
@@ -342,33 +347,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* v_empty = v_full + kVStages;
   uint64_t* s_full = v_empty + kVStages;  // [2]: S_h of the current unit is in TMEM
   uint64_t* p_full = s_full + 2;          // [2]: P_h of the current unit is in TMEM
-  uint64_t* o_full = p_full + 2;          // all products done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_full + 1);
+  uint64_t* o_full = p_full + 2;          // [2]: all products of half h done
+  uint64_t* turn = o_full + 2;            // [2]: half h may issue its next group
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(turn + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
-  const TileDesc td = a.tiles[blockIdx.x];
-  const int hkv = blockIdx.y;
+  // one CTA per (tile, KV head), KV head innermost: blocks start in tile
+  // order, and the planner lists tiles longest first
+  const TileDesc td = a.tiles[blockIdx.x / a.Hkv];
+  const int hkv = (int)(blockIdx.x % a.Hkv);
   const SegDesc sd = a.segs[td.seg];
   const int n_units = td.u_hi - td.u_lo;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.G;
   const bool has_b = td.nt > kHalf / G;  // half B holds at least one token
 
+  const int n_halves = has_b ? 2 : 1;
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    // a K / V stage is free once every half's products that read it are done
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(&k_full[s], 1);
-      mbar_init(&k_empty[s], 1);
+      mbar_init(&k_empty[s], (uint32_t)n_halves);
     }
     for (int s = 0; s < kVStages; ++s) {
       mbar_init(&v_full[s], 1);
-      mbar_init(&v_empty[s], 1);
+      mbar_init(&v_empty[s], (uint32_t)n_halves);
     }
     for (int h = 0; h < 2; ++h) {
       mbar_init(&s_full[h], 1);
       mbar_init(&p_full[h], 128);
+      mbar_init(&o_full[h], 1);
+      mbar_init(&turn[h], 1);
     }
-    mbar_init(o_full, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -456,77 +467,80 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (issued[i] >= 0) mbar_wait(&full[i], (uint32_t)issued[i], nullptr);
       }
     }
-  } else if (warp == 9) {
-    if (lane == 0 && n_units > 0) {
-      // ---------------- MMA issuer ----------------
-      // Per unit j, in tensor-pipe order: PV_A(j-1), QK_A(j), PV_B(j-1), QK_B(j).
-      // QK_h(j) overwrites S_h, where P_h(j-1) lives, only after PV_h(j-1)
-      // (in-order pipe); the commit after QK_h(j) therefore also tells the
-      // softmax that PV_h(j-1) is done and O_h may be rescaled.
+  } else if (warp == 9 || warp == 11) {
+    const int h = warp == 9 ? 0 : 1;
+    if (lane == 0 && n_units > 0 && h < n_halves) {
+      // ---------------- MMA issuer of half h ----------------
+      // Group g of half h = PV_h(g-1) (g > 0) then QK_h(g) (g < n_units).
+      // The halves take turns on the tensor pipe, A0 B0 A1 B1 ..., so one
+      // half's softmax always overlaps the other half's products.  An issuer
+      // does its data waits (P, V, K) while the other half's group runs and
+      // then waits only for its turn: the pipe holds about one product at a
+      // time, so every wait between two issues would leave it idle.  QK_h(g)
+      // overwrites S_h, where P_h(g-1) lives, only after PV_h(g-1) (same
+      // thread, in order); the commit after QK_h(g) covers PV_h(g-1) too, so
+      // it also tells the softmax that O_h is stable and may be rescaled.
       const uint32_t idesc_qk = umma_idesc_bf16_f32(kHalf, kKeysPerUnit);
       const uint32_t idesc_pv = umma_idesc_bf16_f32(kHalf, D) | (1u << 16);  // B (V) MN-major
-      const uint32_t q_addr = smem_u32(sQ);
-      const int n_halves = has_b ? 2 : 1;
+      const uint32_t q_addr = smem_u32(sQ) + (uint32_t)(h * C::kQHalf);
+      const uint32_t s_col = tmem + C::kColS + (uint32_t)(h * kKeysPerUnit);
+      const uint32_t o_col = tmem + C::kColO + (uint32_t)(h * D);
+      const bool paired = n_halves == 2;
       bool ok = mbar_wait(q_full, 0, abort_flag);
       int ks = 0, vs = 0;
       uint32_t kph = 0, vph = 0;
-      auto pv = [&](int h, int j) -> bool {
-        if (!mbar_wait(&p_full[h], (uint32_t)(j & 1), abort_flag)) return false;
-        if (h == 0 && !mbar_wait(&v_full[vs], vph, abort_flag)) return false;
+      for (int g = 0; g <= n_units && ok; ++g) {
+        const bool do_pv = g > 0, do_qk = g < n_units;
+        // data waits first
+        if (do_pv) ok = mbar_wait(&p_full[h], (uint32_t)((g - 1) & 1), abort_flag) &&
+                        mbar_wait(&v_full[vs], vph, abort_flag);
+        if (ok && do_qk) ok = mbar_wait(&k_full[ks], kph, abort_flag);
+        // then the turn: A's group g after B's group g-1, B's group g after A's group g
+        if (ok && paired && (h == 1 || g > 0))
+          ok = mbar_wait(&turn[h], (uint32_t)((h == 0 ? g - 1 : g) & 1), abort_flag);
+        if (!ok) break;
         tc_fence_after();
-        const uint32_t v_addr = smem_u32(sV + vs * C::kV);
-        const uint32_t p_col = tmem + C::kColS + (uint32_t)(h * kKeysPerUnit);
-        const uint32_t o_col = tmem + C::kColO + (uint32_t)(h * D);
+        if (do_pv) {
+          const uint32_t v_addr = smem_u32(sV + vs * C::kV);
 #pragma unroll
-        for (int p = 0; p < kPages; ++p)
-          umma_bf16_tmem_a(o_col, p_col + 8 * p,
-                           umma_desc_mn_sw128(v_addr + p * (kPageSize * 128), C::kKSlab), idesc_pv,
-                           (j > 0 || p > 0) ? 1u : 0u);
-        if (h == n_halves - 1) {
+          for (int p = 0; p < kPages; ++p)
+            umma_bf16_tmem_a(o_col, s_col + 8 * p,
+                             umma_desc_mn_sw128(v_addr + p * (kPageSize * 128), C::kKSlab), idesc_pv,
+                             (g > 1 || p > 0) ? 1u : 0u);
+        }
+        if (do_qk) {
+          const uint32_t k_addr = smem_u32(sK + ks * C::kK);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t qo = (kk >> 2) * C::kQSlab + (kk & 3) * 32;
+            const uint32_t ko = (kk >> 2) * C::kKSlab + (kk & 3) * 32;
+            umma_bf16(s_col, umma_desc_k_sw128(q_addr + qo), umma_desc_k_sw128(k_addr + ko),
+                      idesc_qk, kk > 0 ? 1u : 0u);
+          }
+        }
+        if (paired) mbar_arrive(&turn[h ^ 1]);
+        if (do_pv) {
           umma_commit(&v_empty[vs]);
           if (++vs == kVStages) {
             vs = 0;
             vph ^= 1;
           }
         }
-        return true;
-      };
-      for (int it = 0; it < n_units && ok; ++it) {
-        for (int h = 0; h < n_halves; ++h) {
-          if (it > 0 && !pv(h, it - 1)) {
-            ok = false;
-            break;
-          }
-          if (h == 0 && !mbar_wait(&k_full[ks], kph, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t k_addr = smem_u32(sK + ks * C::kK);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t qo = h * C::kQHalf + (kk >> 2) * C::kQSlab + (kk & 3) * 32;
-            const uint32_t ko = (kk >> 2) * C::kKSlab + (kk & 3) * 32;
-            umma_bf16(tmem + C::kColS + (uint32_t)(h * kKeysPerUnit), umma_desc_k_sw128(q_addr + qo),
-                      umma_desc_k_sw128(k_addr + ko), idesc_qk, kk > 0 ? 1u : 0u);
-          }
+        if (do_qk) {
           umma_commit(&s_full[h]);
-          if (h == n_halves - 1) {
-            umma_commit(&k_empty[ks]);
-            if (++ks == kKStages) {
-              ks = 0;
-              kph ^= 1;
-            }
+          umma_commit(&k_empty[ks]);
+          if (++ks == kKStages) {
+            ks = 0;
+            kph ^= 1;
           }
         }
       }
-      for (int h = 0; h < n_halves && ok; ++h) ok = pv(h, n_units - 1);
       if (!ok) {
         if (!*abort_flag) raise_error(a.err, kErrTimeout);
         *abort_flag = 1;
       }
-      umma_commit(o_full);  // every product issued so far, also on the abort path
-      mbar_wait(o_full, 0, nullptr);
+      umma_commit(&o_full[h]);  // every product of this half, also on the abort path
+      mbar_wait(&o_full[h], 0, nullptr);
     }
   } else if (warp < 8 && n_units > 0 && (warp < 4 || has_b)) {
     // ---------------- softmax / epilogue of one half ----------------
@@ -608,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&p_full[h]);
       walk.next(a, sd, td);
     }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_full, 0, abort_flag));
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&o_full[h], 0, abort_flag));
     if (!ok) {
       if (!*abort_flag) raise_error(a.err, kErrTimeout);
       *abort_flag = 1;
@@ -834,7 +848,7 @@ cudaError_t run_call(const AttnLaunch& L) {
     cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)L.n_tiles, (unsigned)L.Hkv);
+    const dim3 grid((unsigned)L.n_tiles * (unsigned)L.Hkv);
     attn_tc_kernel<D><<<grid, kThreads, smem, st>>>(tmQ, tmKr, tmK1, tmVr, tmV1, a);
     ++launches;
   }
