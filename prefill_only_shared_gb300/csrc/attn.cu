@@ -348,8 +348,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* s_full = v_empty + kVStages;  // [2]: S_h of the current unit is in TMEM
   uint64_t* p_full = s_full + 2;          // [2]: P_h of the current unit is in TMEM
   uint64_t* o_full = p_full + 2;          // [2]: all products of half h done
-  uint64_t* turn = o_full + 2;            // [2]: half h may issue its next group
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(turn + 2);
+  uint64_t* first_turn = o_full + 2;      // half A issued its first group
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(first_turn + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   // one CTA per (tile, KV head), KV head innermost: blocks start in tile
@@ -374,12 +374,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], (uint32_t)n_halves);
     }
+    // p_full[h] phase m: the 4 warps of half h have written P_h(m) to TMEM and, with two
+    // halves, the other half's issuer has issued the group before half h's
+    // next one (its turn on the tensor pipe)
     for (int h = 0; h < 2; ++h) {
       mbar_init(&s_full[h], 1);
-      mbar_init(&p_full[h], 128);
+      mbar_init(&p_full[h], 4u + (n_halves == 2 ? 1u : 0u));
       mbar_init(&o_full[h], 1);
-      mbar_init(&turn[h], 1);
     }
+    mbar_init(first_turn, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -491,22 +494,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t kph = 0, vph = 0;
       for (int g = 0; g <= n_units && ok; ++g) {
         const bool do_pv = g > 0, do_qk = g < n_units;
-        // data waits first
-        if (do_pv) ok = mbar_wait(&p_full[h], (uint32_t)((g - 1) & 1), abort_flag) &&
-                        mbar_wait(&v_full[vs], vph, abort_flag);
-        if (ok && do_qk) ok = mbar_wait(&k_full[ks], kph, abort_flag);
-        // then the turn: A's group g after B's group g-1, B's group g after A's group g
-        if (ok && paired && (h == 1 || g > 0))
-          ok = mbar_wait(&turn[h], (uint32_t)((h == 0 ? g - 1 : g) & 1), abort_flag);
+        // K and V are usually in place already; P_h(g-1) together with the
+        // turn (A's group g after B's group g-1, B's group g after A's group
+        // g) is one barrier phase, the only wait that is usually not over
+        if (do_qk) ok = mbar_wait(&k_full[ks], kph, abort_flag);
+        if (ok && do_pv) ok = mbar_wait(&v_full[vs], vph, abort_flag);
+        if (ok && do_pv) ok = mbar_wait_poll(&p_full[h], (uint32_t)((g - 1) & 1), abort_flag);
+        if (ok && paired && h == 1 && g == 0) ok = mbar_wait_poll(first_turn, 0, abort_flag);
         if (!ok) break;
         tc_fence_after();
         if (do_pv) {
           const uint32_t v_addr = smem_u32(sV + vs * C::kV);
 #pragma unroll
-          for (int p = 0; p < kPages; ++p)
+          for (int p = 0; p < kPages; ++p) {
             umma_bf16_tmem_a(o_col, s_col + 8 * p,
                              umma_desc_mn_sw128(v_addr + p * (kPageSize * 128), C::kKSlab), idesc_pv,
                              (g > 1 || p > 0) ? 1u : 0u);
+          }
         }
         if (do_qk) {
           const uint32_t k_addr = smem_u32(sK + ks * C::kK);
@@ -518,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       idesc_qk, kk > 0 ? 1u : 0u);
           }
         }
-        if (paired) mbar_arrive(&turn[h ^ 1]);
+        if (paired) mbar_arrive(h == 1 ? &p_full[0] : (g == 0 ? first_turn : &p_full[1]));
         if (do_pv) {
           umma_commit(&v_empty[vs]);
           if (++vs == kVStages) {
@@ -558,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     walk.start(a, sd, td);
     bool ok = true;
     for (int it = 0; it < n_units; ++it) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[h], (uint32_t)(it & 1), abort_flag))) {
+      if (!__all_sync(0xffffffffu, mbar_wait_poll(&s_full[h], (uint32_t)(it & 1), abort_flag))) {
         ok = false;
         break;
       }
@@ -619,7 +623,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // P_h (bf16 pairs) over the first 64 columns of S_h
       tmem_st64(trow + s_col, pw);
       tc_fence_before();
-      mbar_arrive(&p_full[h]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[h]);  // one arrival per warp
       walk.next(a, sd, td);
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&o_full[h], 0, abort_flag));

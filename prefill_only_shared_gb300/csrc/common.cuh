@@ -62,6 +62,34 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait without a suspend hint: the thread polls, and sees the phase
+// complete as soon as it does (for waits on the critical path).
+__device__ __forceinline__ bool mbar_try_wait_poll(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded polling wait (see mbar_wait), for the waits on the critical path.
+__device__ __forceinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity,
+                                               volatile int* abort_flag) {
+  if (mbar_try_wait_poll(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait_poll(bar, parity)) return true;
+    if ((i & 255u) == 0) {
+      if (abort_flag && *abort_flag) return false;
+      if (globaltimer() - t0 > kWaitLimitNs) return false;
+    }
+  }
+}
+
 // Bounded wait for the phase with the given parity.  Returns false when the
 // limit passed or *abort became non-zero (another role gave up).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
