@@ -109,6 +109,84 @@ EncodeTiledFn get_encode_tiled() {
   });
   return fn;
 }
+
+// A tensor map is a host-side encoding of (base, shape, strides, box,
+// swizzle): calls that pass the same buffers reuse the encoded map from a
+// small per-thread table instead of encoding it again.
+namespace {
+struct MapKey {
+  const void* base;
+  uint32_t rank, dtype, swz, l2;
+  cuuint64_t dims[5];
+  cuuint64_t strides[4];
+  cuuint32_t box[5];
+};
+struct MapEntry {
+  MapKey key;
+  CUtensorMap map;
+  bool valid;
+};
+constexpr int kMapCache = 32;
+}  // namespace
+
+bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, const void* base,
+                  const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                  CUtensorMapSwizzle swz, CUtensorMapL2promotion l2) {
+  if (rank < 1 || rank > 5) return false;
+  MapKey k;
+  std::memset(&k, 0, sizeof(k));
+  k.base = base;
+  k.rank = rank;
+  k.dtype = (uint32_t)dtype;
+  k.swz = (uint32_t)swz;
+  k.l2 = (uint32_t)l2;
+  for (uint32_t i = 0; i < rank; ++i) {
+    k.dims[i] = dims[i];
+    k.box[i] = box[i];
+    if (i + 1 < rank) k.strides[i] = strides[i];
+  }
+  thread_local MapEntry cache[kMapCache];
+  thread_local int next = 0;
+  for (int i = 0; i < kMapCache; ++i)
+    if (cache[i].valid && std::memcmp(&cache[i].key, &k, sizeof(k)) == 0) {
+      *map = cache[i].map;
+      return true;
+    }
+  EncodeTiledFn enc = get_encode_tiled();
+  if (!enc) return false;
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  if (enc(map, dtype, rank, const_cast<void*>(base), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, swz, l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  MapEntry& e = cache[next];
+  next = (next + 1) % kMapCache;
+  e.key = k;
+  e.map = *map;
+  e.valid = true;
+  return true;
+}
+
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per kernel and device.
+cudaError_t ensure_dynamic_smem(const void* func, int bytes) {
+  struct Done {
+    const void* func;
+    int dev;
+    int bytes;
+  };
+  static std::mutex mu;
+  static Done done[64];
+  static int n_done = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n_done; ++i)
+    if (done[i].func == func && done[i].dev == dev && done[i].bytes >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  if (n_done < 64) done[n_done++] = Done{func, dev, bytes};
+  return cudaSuccess;
+}
 }  // namespace sp
 
 extern "C" sp_status sp_plan_upload(const sp_plan* plan, void* dev_desc, size_t bytes,

@@ -773,12 +773,8 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const SegDesc* segs, con
 
 bool encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
             const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swz) {
-  EncodeTiledFn enc = get_encode_tiled();
-  if (!enc) return false;
-  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), dims,
-             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (uint32_t)rank, base, dims, strides,
+                      box, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
 template <int D>
@@ -850,8 +846,7 @@ cudaError_t run_call(const AttnLaunch& L) {
     a.G = G;
     a.scale_log2 = 1.4426950408889634f / sqrtf((float)D);
     const size_t smem = Cfg<D>::kSmem;
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(attn_tc_kernel<D>), (int)smem);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)L.n_tiles * (unsigned)L.Hkv);
     attn_tc_kernel<D><<<grid, kThreads, smem, st>>>(tmQ, tmKr, tmK1, tmVr, tmV1, a);

@@ -81,4 +81,13 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn get_encode_tiled();
 
+// cuTensorMapEncodeTiled with element strides 1, no interleave, no OOB fill
+// override, through a per-thread cache of recent encodings.
+bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, const void* base,
+                  const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                  CUtensorMapSwizzle swz, CUtensorMapL2promotion l2);
+
+// Raise a kernel's dynamic shared memory limit, once per kernel and device.
+cudaError_t ensure_dynamic_smem(const void* func, int bytes);
+
 }  // namespace sp

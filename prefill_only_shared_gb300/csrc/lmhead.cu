@@ -336,16 +336,11 @@ Geometry geometry(int N, int V, int n_sms) {
 
 bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_in,
                uint32_t box_out) {
-  EncodeTiledFn enc = get_encode_tiled();
-  if (!enc) return false;
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {inner * 2};
   cuuint32_t box[2] = {box_in, box_out};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
 }  // namespace
@@ -379,8 +374,7 @@ cudaError_t lmhead_run(const LmheadLaunch& L) {
   a.grid_arrivals = reinterpret_cast<unsigned*>(a.partials + (size_t)g.grid * L.N);
   a.lse = L.lse;
   a.err = L.err;
-  cudaError_t e = cudaFuncSetAttribute(lmhead_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)g.smem);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(lmhead_kernel), (int)g.smem);
   if (e != cudaSuccess) return e;
   cudaStream_t st = static_cast<cudaStream_t>(L.stream);
   e = cudaMemsetAsync(a.grid_arrivals, 0, sizeof(unsigned), st);

@@ -40,6 +40,9 @@ class SharedPrefixClassifier:
         self.fixed_pool = max_pages is not None
         self.n_sms = torch.cuda.get_device_properties(self.device).multi_processor_count
         self._bufs = {}
+        self._views = {}
+        self._lm_ws_key = None
+        self._lm_ws_bytes = 0
         self.kv_pool = None
         self._ensure_pool(int(max_pages) if max_pages is not None else 0)
 
@@ -55,11 +58,28 @@ class SharedPrefixClassifier:
         return self.kv_pool.shape[0] if self.fixed_pool else (1 << 31) - 1
 
     def _buf(self, name, numel, dtype):
+        """A view of `numel` elements of the grow-only buffer `name` (views are
+        reused while the buffer stays)."""
+        key = (name, int(numel), dtype)
+        view = self._views.get(key)
+        if view is not None:
+            return view
         b = self._bufs.get(name)
         if b is None or b.numel() < numel or b.dtype != dtype:
             b = torch.empty(max(int(numel), 1), dtype=dtype, device=self.device)
             self._bufs[name] = b
-        return b[:max(int(numel), 1)] if numel else b[:0]
+            self._views = {k: v for k, v in self._views.items() if k[0] != name}
+        view = b[:max(int(numel), 1)] if numel else b[:0]
+        self._views[key] = view
+        return view
+
+    def _stream(self, stream):
+        """Raw cudaStream_t of `stream` (None: torch's current stream)."""
+        if stream is None:
+            return torch.cuda.current_stream(self.device).cuda_stream
+        if isinstance(stream, torch.cuda.Stream):
+            return stream.cuda_stream
+        return int(stream)
 
     def plan(self, req_of_branch, tok_offsets, tokens) -> "sp.Plan":
         plan = sp.sp_plan_build(self.shape, req_of_branch, tok_offsets, tokens, self.max_pages,
@@ -71,12 +91,11 @@ class SharedPrefixClassifier:
         """schedule "rounds": one prefix and one branch call per staged round,
         in round order; "all": one prefix call and one branch call covering
         every round (same results, fewer launches)."""
+        stream = self._stream(stream)
         st = plan.stats()
         T = st["node_tokens"]
         Hq, d = self.shape.n_q_heads, self.shape.head_dim
-        desc = self._buf("desc", st["desc_bytes"] + 256, torch.uint8)
-        off = (-desc.data_ptr()) % 256
-        desc = desc[off:off + st["desc_bytes"]] if off else desc[:st["desc_bytes"]]
+        desc = self._desc_view(st["desc_bytes"])
         sp.sp_plan_upload(plan, desc, stream)
         ws = self._buf("attn_ws", st["attn_workspace_bytes"], torch.uint8)
         out = self._buf("out", T * Hq * d, torch.bfloat16).view(T, Hq, d)
@@ -91,9 +110,25 @@ class SharedPrefixClassifier:
         self.last_attention_launches = launches
         return out, lse
 
+    def _desc_view(self, nbytes):
+        """A 256-byte-aligned device view of `nbytes` for the plan descriptor."""
+        key = ("desc", -int(nbytes), "aligned")  # dropped with the "desc" buffer
+        view = self._views.get(key)
+        if view is None:
+            raw = self._buf("desc", nbytes + 256, torch.uint8)
+            off = (-raw.data_ptr()) % 256
+            view = raw[off:off + nbytes]
+            self._views[key] = view
+        return view
+
     def logprobs(self, h, W, label_off, label_ids, n_labels, stream=None):
+        stream = self._stream(stream)
         N = h.shape[0]
-        ws = self._buf("lm_ws", sp.sp_label_workspace_bytes(N, W.shape[0], self.n_sms), torch.uint8)
+        wkey = (N, W.shape[0])
+        if self._lm_ws_key != wkey:
+            self._lm_ws_bytes = sp.sp_label_workspace_bytes(N, W.shape[0], self.n_sms)
+            self._lm_ws_key = wkey
+        ws = self._buf("lm_ws", self._lm_ws_bytes, torch.uint8)
         logprobs = self._buf("logprobs", n_labels, torch.float32)
         lse = self._buf("lse_vocab", N, torch.float32)
         sp.sp_label_logprobs(h, W, label_off, label_ids, n_labels, logprobs, lse, ws, stream)
@@ -101,6 +136,7 @@ class SharedPrefixClassifier:
         return logprobs, lse
 
     def softmax(self, logprobs, label_off, stream=None):
+        stream = self._stream(stream)
         N = label_off.numel() - 1
         probs = self._buf("probs", logprobs.numel(), torch.float32)
         argmax = self._buf("argmax", N, torch.int32)
@@ -112,6 +148,7 @@ class SharedPrefixClassifier:
         """One question per branch, its options the branch's labels: label
         softmax fused with the question type's value and the confidence.
         Returns (probs, argmax, value, confidence)."""
+        stream = self._stream(stream)
         N = label_off.numel() - 1
         probs = self._buf("probs", logprobs.numel(), torch.float32)
         argmax = self._buf("argmax", N, torch.int32)
@@ -124,6 +161,7 @@ class SharedPrefixClassifier:
     def candidates(self, probs, label_off, cand_off, qtype, stream=None):
         """Questions assembled from yes/no candidate branches (consecutive
         branches per question).  Returns (dist, argmax, value, confidence)."""
+        stream = self._stream(stream)
         Q = cand_off.numel() - 1
         dist = self._buf("dist", label_off.numel() - 1, torch.float32)  # >= cand_off[-1]
         argmax = self._buf("q_argmax", Q, torch.int32)
@@ -137,6 +175,7 @@ class SharedPrefixClassifier:
         """LM-head label log-probabilities, then the label softmax; with
         ``qtype`` (device int32 [N]) the softmax is the fused decision and the
         value / confidence are returned too (else None)."""
+        stream = self._stream(stream)
         logprobs, lse = self.logprobs(h, W, label_off, label_ids, n_labels, stream)
         value = conf = None
         if qtype is None:
@@ -149,6 +188,7 @@ class SharedPrefixClassifier:
     def run(self, req_of_branch, tok_offsets, tokens, q, k, v, h, W, label_off, label_ids,
             stream=None, schedule="rounds", qtype=None) -> PassOutputs:
         """q/k/v in node-token order of the plan (see sp_plan_segments)."""
+        stream = self._stream(stream)
         plan = self.plan(req_of_branch, tok_offsets, tokens)
         out, lse = self.attention(plan, q, k, v, stream, schedule)
         n_labels = int(label_ids.numel())

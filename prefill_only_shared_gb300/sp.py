@@ -117,6 +117,10 @@ def _check(status: int, where: str):
 
 
 def _stream(stream):
+    """A cudaStream_t from None (torch's current stream), a torch stream or a
+    raw handle (int)."""
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
     if stream is None:
         return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     if isinstance(stream, torch.cuda.Stream):
@@ -144,6 +148,7 @@ class Plan:
     def __init__(self, ptr: ctypes.c_void_p, shape: sp_shape):
         self._ptr = ptr
         self.shape = shape
+        self._stats = None
 
     @property
     def ptr(self):
@@ -161,9 +166,12 @@ class Plan:
             pass
 
     def stats(self) -> dict:
-        st = sp_plan_stats()
-        _check(lib().sp_plan_get_stats(self._ptr, ctypes.byref(st)), "sp_plan_get_stats")
-        return st.as_dict()
+        """Token and launch accounting (a plan is immutable: read once)."""
+        if self._stats is None:
+            st = sp_plan_stats()
+            _check(lib().sp_plan_get_stats(self._ptr, ctypes.byref(st)), "sp_plan_get_stats")
+            self._stats = st.as_dict()
+        return dict(self._stats)
 
     def rounds(self) -> list:
         n = _I32()
