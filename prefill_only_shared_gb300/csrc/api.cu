@@ -64,13 +64,13 @@ sp_status attn_call(const sp_plan* P, const void* dev_desc, int32_t round, int k
   sp::AttnLaunch L;
   L.hdr = &P->hdr;
   L.dev_desc = dev_desc;
-  L.append_off = c.append_off;
-  L.n_append = c.n_append;
   L.tile_off = c.tile_off;
   L.n_tiles = c.n_tiles;
   L.merge_off = c.merge_off;
   L.n_merges = c.n_merges;
   L.n_parts = c.n_parts;
+  L.round = round;
+  L.kind = kind;
   L.q = q;
   L.k = k;
   L.v = v;

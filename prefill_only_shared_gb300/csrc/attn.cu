@@ -73,6 +73,11 @@ struct AttnArgs {
   const int32_t* page_ids;
   const int32_t* chain;
   const TileDesc* tiles;
+  const bf16* k_in;  // k / v inputs [node_tokens][Hkv][D]
+  const bf16* v_in;
+  bf16* pool;        // [page][K: Hkv x 16 x D | V: Hkv x 16 x D]
+  int call_round;    // round of this call, -1 for all rounds
+  int call_kind;     // 0 prefix (shared segments), 1 branch (leaves)
   bf16* out;
   float* lse;
   float* part_o;
@@ -254,14 +259,23 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 // Walks the KV units of a tile: ancestor levels (root first), then the own
 // segment up to the tile's causal bound.
+// A segment computed by this call has its K/V in the k / v inputs only (the
+// call writes shared segments into the pool for later calls); every other
+// segment was computed by an earlier call and is read from the pool.
+__device__ __forceinline__ bool computed_here(const AttnArgs& a, const SegDesc& x) {
+  return (x.shared != 0) == (a.call_kind == 0) && (a.call_round < 0 || x.round == a.call_round);
+}
+
 struct Cursor {
-  int level;     // 0..chain_len (chain_len = own segment)
-  int j;         // unit within the level
-  int n_units;   // units in this level
-  int len;       // visible keys in this level (own: t0 + nt)
-  int n_pages;   // pages the level's segment owns (page-table bound)
-  int page_off;  // first page-table entry of the level's segment
+  int level;      // 0..chain_len (chain_len = own segment)
+  int j;          // unit within the level
+  int n_units;    // units in this level
+  int len;        // visible keys in this level (own: t0 + nt)
+  int n_pages;    // pages the level's segment owns (page-table bound)
+  int page_off;   // first page-table entry of the level's segment
+  int64_t row0;   // the level's first row in the k / v inputs
   bool own;
+  bool local;     // read from the k / v inputs, not from the pool
 };
 
 __device__ __forceinline__ void cursor_level(Cursor& c, const AttnArgs& a, const SegDesc& sd,
@@ -271,12 +285,16 @@ __device__ __forceinline__ void cursor_level(Cursor& c, const AttnArgs& a, const
     c.len = an.len;
     c.n_pages = (an.len + kPageSize - 1) / kPageSize;
     c.page_off = an.page_off;
+    c.row0 = an.node_start;
     c.own = false;
+    c.local = computed_here(a, an);
   } else {
     c.len = td.t0 + td.nt;
     c.n_pages = (sd.len + kPageSize - 1) / kPageSize;
     c.page_off = sd.page_off;
+    c.row0 = sd.node_start;
     c.own = true;
+    c.local = computed_here(a, sd);
   }
   c.n_units = (c.len + kKeysPerUnit - 1) / kKeysPerUnit;
 }
@@ -332,7 +350,8 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKr,
                    const __grid_constant__ CUtensorMap tmK1, const __grid_constant__ CUtensorMap tmVr,
-                   const __grid_constant__ CUtensorMap tmV1, AttnArgs a) {
+                   const __grid_constant__ CUtensorMap tmV1, const __grid_constant__ CUtensorMap tmKi,
+                   const __grid_constant__ CUtensorMap tmVi, AttnArgs a) {
   using C = Cfg<D>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = align1024(smem_raw);
@@ -403,6 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensormap(&tmQ);
         prefetch_tensormap(&tmKr);
         prefetch_tensormap(&tmK1);
+        prefetch_tensormap(&tmKi);
         mbar_expect_tx(q_full, (uint32_t)(2 * C::kQHalf));
         for (int h = 0; h < 2; ++h)
           for (int slab = 0; slab < D / 64; ++slab)
@@ -412,6 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!is_k && lane == 0) {
         prefetch_tensormap(&tmVr);
         prefetch_tensormap(&tmV1);
+        prefetch_tensormap(&tmVi);
       }
       const int n_st = is_k ? kKStages : kVStages;
       uint64_t* full = is_k ? k_full : v_full;
@@ -445,7 +466,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_expect_tx(&full[s], bytes);
         __syncwarp();
         unsigned char* dst = is_k ? sK + s * C::kK : sV + s * C::kV;
-        if (run) {
+        if (walk.cur.local) {
+          // 128 consecutive rows of the inputs: one box per 64-dim slab (rows
+          // past the level's end are masked by the softmax)
+          if (lane == 0)
+            for (int slab = 0; slab < D / 64; ++slab)
+              tma_load_3d(dst + slab * C::kKSlab, is_k ? &tmKi : &tmVi, &full[s], slab * 64, hkv,
+                          (int32_t)(walk.cur.row0 + (int64_t)walk.cur.j * kKeysPerUnit));
+        } else if (run) {
           if (lane == 0)
             for (int slab = 0; slab < D / 64; ++slab)
               tma_load_4d(dst + slab * C::kKSlab, is_k ? &tmKr : &tmVr, &full[s], slab * 64, 0, hkv, p0);
@@ -468,6 +496,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (is_k) mbar_wait(q_full, 0, nullptr);
         for (int i = 0; i < n_st; ++i)
           if (issued[i] >= 0) mbar_wait(&full[i], (uint32_t)issued[i], nullptr);
+      }
+      // A shared segment computed here goes into the pool for later calls:
+      // the first part of each tile copies the tile's tokens for its KV head
+      // (warp 8 the K rows, warp 10 the V rows), and the tile holding the
+      // segment's last token zero-fills the rest of that page.  No tile of
+      // this call reads these pages.
+      if (ok && td.u_lo == 0 && sd.shared && computed_here(a, sd)) {
+        constexpr int kChunks = D / 8;  // 16-byte chunks per row
+        const bf16* src = is_k ? a.k_in : a.v_in;
+        const size_t page_elems = (size_t)2 * a.Hkv * kPageSize * D;
+        const size_t kv_off = ((size_t)(is_k ? 0 : a.Hkv) + hkv) * kPageSize * D;
+        const int t_end = td.t0 + td.nt;
+        const int t_fill = t_end == sd.len ? ((sd.len + kPageSize - 1) / kPageSize) * kPageSize : t_end;
+        const int n_items = (t_fill - td.t0) * kChunks;
+        constexpr int kBatch = 8;  // loads in flight per lane before the stores
+        for (int i0 = 0; i0 < n_items; i0 += 32 * kBatch) {
+          uint4 val[kBatch];
+#pragma unroll
+          for (int b = 0; b < kBatch; ++b) {
+            const int i = i0 + b * 32 + lane;
+            const int t = td.t0 + i / kChunks, ch = i % kChunks;
+            val[b] = make_uint4(0, 0, 0, 0);
+            if (i < n_items && t < t_end)
+              val[b] = *reinterpret_cast<const uint4*>(
+                  src + ((size_t)(sd.node_start + t) * a.Hkv + hkv) * D + ch * 8);
+          }
+#pragma unroll
+          for (int b = 0; b < kBatch; ++b) {
+            const int i = i0 + b * 32 + lane;
+            if (i >= n_items) break;
+            const int t = td.t0 + i / kChunks, ch = i % kChunks;
+            const int page = a.page_ids[sd.page_off + t / kPageSize];
+            *reinterpret_cast<uint4*>(a.pool + (size_t)page * page_elems + kv_off +
+                                      (size_t)(t % kPageSize) * D + ch * 8) = val[b];
+          }
+        }
       }
     }
   } else if (warp == 9 || warp == 11) {
@@ -742,35 +806,6 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const SegDesc* segs, co
   if (lane == 0) lse_out[orow] = S > 0.f ? M + __logf(S) : -INFINITY;
 }
 
-// Copy the K/V of one 16-token page of a segment, for one KV head (grid.y),
-// into its pool page.  Pool page layout: K as [Hkv][16][D], then V as
-// [Hkv][16][D]; slots past the segment end are zero-filled.
-template <int D>
-__global__ void __launch_bounds__(256) kv_append_kernel(const SegDesc* segs, const int32_t* page_ids,
-                                                        const AppendDesc* app, const bf16* k,
-                                                        const bf16* v, bf16* pool, int Hkv) {
-  constexpr int CPR = D / 8;
-  const AppendDesc ad = app[blockIdx.x];
-  const int h = blockIdx.y;
-  const SegDesc sd = segs[ad.seg];
-  const int tok0 = ad.page_in_seg * kPageSize;
-  const int ntok = min(kPageSize, sd.len - tok0);
-  const int page = page_ids[sd.page_off + ad.page_in_seg];
-  const size_t kbase = (((size_t)page * 2) * Hkv + h) * kPageSize * D;
-  const size_t vbase = (((size_t)page * 2 + 1) * Hkv + h) * kPageSize * D;
-  for (int i = threadIdx.x; i < kPageSize * CPR; i += blockDim.x) {
-    const int ch = i % CPR, slot = i / CPR;
-    uint4 kk = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
-    if (slot < ntok) {
-      const size_t src = ((size_t)(sd.node_start + tok0 + slot) * Hkv + h) * D + ch * 8;
-      kk = *reinterpret_cast<const uint4*>(k + src);
-      vv = *reinterpret_cast<const uint4*>(v + src);
-    }
-    *reinterpret_cast<uint4*>(pool + kbase + (size_t)slot * D + ch * 8) = kk;
-    *reinterpret_cast<uint4*>(pool + vbase + (size_t)slot * D + ch * 8) = vv;
-  }
-}
-
 bool encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
             const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swz) {
   return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (uint32_t)rank, base, dims, strides,
@@ -784,23 +819,25 @@ cudaError_t run_call(const AttnLaunch& L) {
   const SegDesc* segs = reinterpret_cast<const SegDesc*>(base + h.off_segs);
   const int32_t* pages = reinterpret_cast<const int32_t*>(base + h.off_pages);
   const int32_t* chain = reinterpret_cast<const int32_t*>(base + h.off_chain);
-  const AppendDesc* app =
-      reinterpret_cast<const AppendDesc*>(base + h.off_append) + L.append_off;
   const TileDesc* tiles = reinterpret_cast<const TileDesc*>(base + h.off_tiles) + L.tile_off;
   const MergeDesc* merges = reinterpret_cast<const MergeDesc*>(base + h.off_merges) + L.merge_off;
   cudaStream_t st = static_cast<cudaStream_t>(L.stream);
   bf16* pool = static_cast<bf16*>(L.pool);
   const int G = L.Hq / L.Hkv;
   int launches = 0;
-  if (L.n_append > 0) {
-    kv_append_kernel<D><<<dim3((unsigned)L.n_append, (unsigned)L.Hkv), 256, 0, st>>>(
-        segs, pages, app, static_cast<const bf16*>(L.k), static_cast<const bf16*>(L.v), pool, L.Hkv);
-    ++launches;
-  }
   float* part_o = static_cast<float*>(L.workspace);
   float* part_lse = part_o + (size_t)L.n_parts * L.Hkv * kRowsPerTile * D;
   if (L.n_tiles > 0) {
-    CUtensorMap tmQ, tmKr, tmK1, tmVr, tmV1;
+    CUtensorMap tmQ, tmKr, tmK1, tmVr, tmV1, tmKi, tmVi;
+    {
+      // k / v inputs [node_tokens][Hkv][D]: 128 rows of one KV head per box
+      cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)L.Hkv, (cuuint64_t)L.node_tokens};
+      cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)L.Hkv * D * 2};
+      cuuint32_t box[3] = {64, 1, (cuuint32_t)kKeysPerUnit};
+      if (!encode(&tmKi, L.k, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+          !encode(&tmVi, L.v, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    }
     {
       cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)L.Hq, (cuuint64_t)L.node_tokens};
       cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)L.Hq * D * 2};
@@ -836,6 +873,11 @@ cudaError_t run_call(const AttnLaunch& L) {
     a.page_ids = pages;
     a.chain = chain;
     a.tiles = tiles;
+    a.k_in = static_cast<const bf16*>(L.k);
+    a.v_in = static_cast<const bf16*>(L.v);
+    a.pool = pool;
+    a.call_round = L.round;
+    a.call_kind = L.kind;
     a.out = static_cast<bf16*>(L.out);
     a.lse = L.lse;
     a.part_o = part_o;
@@ -849,7 +891,7 @@ cudaError_t run_call(const AttnLaunch& L) {
     cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(attn_tc_kernel<D>), (int)smem);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)L.n_tiles * (unsigned)L.Hkv);
-    attn_tc_kernel<D><<<grid, kThreads, smem, st>>>(tmQ, tmKr, tmK1, tmVr, tmV1, a);
+    attn_tc_kernel<D><<<grid, kThreads, smem, st>>>(tmQ, tmKr, tmK1, tmVr, tmV1, tmKi, tmVi, a);
     ++launches;
   }
   if (L.n_merges > 0) {

@@ -9,23 +9,28 @@ constexpr int kRowsPerTile = 256;  // query rows (token x group-head) per CTA ti
 constexpr int kKeysPerUnit = 128;  // keys per KV unit (8 pages of 16): one N=128 MMA
 constexpr int kPageSize = 16;      // tokens per KV page
 
-// One trie segment.  Its K/V live in pages page_ids[page_off ..]; its
-// ancestors (root first) are chain[chain_off .. chain_off + chain_len).
+// One trie segment.  Its K/V rows are node_start .. node_start + len - 1 of
+// the k / v inputs and, once the call that computes it has run and if it is
+// shared, pages page_ids[page_off ..] of the pool; its ancestors (root first)
+// are chain[chain_off .. chain_off + chain_len).  It is computed in round
+// `round`, by the prefix call when `shared` (an inner trie node: at least
+// two branches pass through it), else by the branch call (a leaf).
 struct SegDesc {
   int64_t node_start;  // first node-token row
   int32_t len;
   int32_t page_off;
   int32_t chain_off;
   int32_t chain_len;
-  int32_t pad0, pad1;
+  int32_t round;
+  int32_t shared;
 };
 
 // One CTA of attention work: tokens [t0, t0+nt) of segment `seg` (times the
-// query heads of one KV head, which is the launch's y index), over the KV
+// query heads of one KV head, the innermost part of the launch index), over the KV
 // units [u_lo, u_hi) of its context (ancestor units first, then own units up
 // to the causal bound).  part < 0: write final out/lse; else write partial
-// slot `part`; the last of the split tile's parts to finish (merge entry
-// `merge` of the call) combines them.
+// slot `part`, which the call's merge entry `merge` combines with the other
+// parts of the split tile.
 struct TileDesc {
   int32_t seg, t0, nt, u_lo, u_hi, part;
   int32_t merge, pad1;
@@ -37,7 +42,8 @@ struct MergeDesc {
   int32_t pad0, pad1, pad2;
 };
 
-// One 16-token page of a segment whose K/V are appended into the pool.
+// One 16-token page of a shared segment that a call writes into the pool
+// (plan metadata: the attention kernel writes the pages of the tiles it runs).
 struct AppendDesc {
   int32_t seg, page_in_seg;
 };

@@ -12,8 +12,10 @@ namespace sp {
 struct AttnLaunch {
   const DescHeader* hdr;
   const void* dev_desc;
-  int64_t append_off, n_append, tile_off, n_tiles, merge_off, n_merges;
+  int64_t tile_off, n_tiles, merge_off, n_merges;
   int32_t n_parts;
+  int32_t round;  // the call's round, -1 for all rounds
+  int32_t kind;   // 0 prefix, 1 branch
   const void* q;
   const void* k;
   const void* v;

@@ -287,7 +287,8 @@ extern "C" sp_status sp_plan_build(const sp_shape* shape, int32_t n_branches,
     segd[s].page_off = P->seg_first_page[s];
     segd[s].chain_off = (int32_t)chain.size();
     segd[s].chain_len = (int32_t)anc.size();
-    segd[s].pad0 = segd[s].pad1 = 0;
+    segd[s].round = P->seg_round[s];
+    segd[s].shared = P->seg_shared[s] ? 1 : 0;
     for (int32_t a : anc) {
       chain.push_back(a);
       anc_units[s] += ceil_div(P->seg_len[a], sp::kKeysPerUnit);
@@ -305,8 +306,9 @@ extern "C" sp_status sp_plan_build(const sp_shape* shape, int32_t n_branches,
   std::vector<sp::MergeDesc> merges;
   int64_t max_parts = 0;
   // calls[2 r + kind] for rounds r < n_rounds; calls[2 n_rounds + kind] run the
-  // work of every round in one call (valid because a call appends all of its
-  // segments' K/V before any of its attention runs).
+  // work of every round in one call.  A call reads the levels it computes
+  // itself from the k / v inputs and every other level from the pool, which
+  // earlier calls have filled, so any grouping of rounds into calls is valid.
   P->calls.resize(2 * (size_t)n_rounds + 2);
   for (int32_t r = 0; r <= n_rounds; ++r) {
     const bool all = r == n_rounds;
@@ -318,8 +320,9 @@ extern "C" sp_status sp_plan_build(const sp_shape* shape, int32_t n_branches,
       for (int32_t s = 0; s < S; ++s) {
         if (!all && P->seg_round[s] != r) continue;
         if ((kind == 0) != (P->seg_shared[s] != 0)) continue;
-        for (int32_t pg = 0; pg < ceil_div(P->seg_len[s], sp::kPageSize); ++pg)
-          appends.push_back({s, pg});
+        if (P->seg_shared[s])  // leaves are read by no later call
+          for (int32_t pg = 0; pg < ceil_div(P->seg_len[s], sp::kPageSize); ++pg)
+            appends.push_back({s, pg});
         for (int32_t t0 = 0; t0 < P->seg_len[s]; t0 += TPT) {
           int32_t nt = std::min(TPT, P->seg_len[s] - t0);
           raw.push_back({s, t0, nt, anc_units[s] + ceil_div(t0 + nt, sp::kKeysPerUnit)});

@@ -1,7 +1,10 @@
 """The planner's device descriptor, checked on the host: a float64 emulation
-of what the attention kernels do with it (append pages into a pool, walk each
-tile's KV units over ancestor and own levels with the causal bound, merge
-split partials) must reproduce the oracle's unshared attention exactly.
+of what the attention kernels do with it (walk each tile's KV units over
+ancestor and own levels with the causal bound, reading a level from the k / v
+inputs when the call computes it and from the pool otherwise; write the
+call's shared segments into the pool after its tiles; merge split partials)
+must reproduce the oracle's unshared attention exactly.  The pool starts as
+NaN, so a level read from the pool before a call has written it shows up.
 
 This pins the work decomposition (pages, chains, units, splits, merges,
 recomputed rows) independently of any GPU arithmetic."""
@@ -17,7 +20,7 @@ from prefill_only_shared_gb300.workloads import make_workload, small_case
 from test_oracle_staging import csr, random_case
 
 SEG = np.dtype([("node_start", "<i8"), ("len", "<i4"), ("page_off", "<i4"), ("chain_off", "<i4"),
-                ("chain_len", "<i4"), ("p0", "<i4"), ("p1", "<i4")])
+                ("chain_len", "<i4"), ("round", "<i4"), ("shared", "<i4")])
 TILE = np.dtype([("seg", "<i4"), ("t0", "<i4"), ("nt", "<i4"), ("u_lo", "<i4"), ("u_hi", "<i4"),
                  ("part", "<i4"), ("merge", "<i4"), ("p1", "<i4")])
 MERGE = np.dtype([("seg", "<i4"), ("t0", "<i4"), ("nt", "<i4"), ("part0", "<i4"), ("nparts", "<i4"),
@@ -51,16 +54,15 @@ def emulate(plan, q, k, v, Hq, Hkv, d, schedule="rounds"):
     for r in (range(st["n_rounds"]) if schedule == "rounds" else [-1]):
         for kind in (0, 1):
             ci = plan.call_info(r, kind)
-            for a in app[ci["append_off"]:ci["append_off"] + ci["n_append"]]:
-                s = segs[a["seg"]]
-                pg = pages[s["page_off"] + a["page"]]
-                for slot in range(PAGE):
-                    t = a["page"] * PAGE + slot
-                    if t < s["len"]:
-                        pool[pg, 0, :, slot] = k[s["node_start"] + t]
-                        pool[pg, 1, :, slot] = v[s["node_start"] + t]
-                    else:
-                        pool[pg, :, :, slot] = 0.0
+
+            def in_call(x):
+                return (x["shared"] == 1) == (kind == 0) and (r < 0 or x["round"] == r)
+
+            # the call writes exactly its shared segments' pages into the pool
+            apps = app[ci["append_off"]:ci["append_off"] + ci["n_append"]]
+            want = sorted((i, p) for i, x in enumerate(segs) if in_call(x) and x["shared"]
+                          for p in range((x["len"] + PAGE - 1) // PAGE))
+            assert sorted((int(a["seg"]), int(a["page"])) for a in apps) == want
             parts = {}
             call_merges = merges[ci["merge_off"]:ci["merge_off"] + ci["n_merges"]]
             for td in tiles[ci["tile_off"]:ci["tile_off"] + ci["n_tiles"]]:
@@ -72,17 +74,20 @@ def emulate(plan, q, k, v, Hq, Hkv, d, schedule="rounds"):
                 else:
                     assert td["merge"] == -1
                 levels = [segs[c] for c in chain[s["chain_off"]:s["chain_off"] + s["chain_len"]]]
-                lv = [(x["page_off"], x["len"], False) for x in levels]
-                lv.append((s["page_off"], td["t0"] + td["nt"], True))
+                lv = [(x, x["len"], False) for x in levels]
+                lv.append((s, td["t0"] + td["nt"], True))
                 keys = []  # (K, V, position within own level or -1)
                 u = 0
-                for page_off, ln, own in lv:
+                for x, ln, own in lv:
                     for j in range((ln + UNIT - 1) // UNIT):
                         if td["u_lo"] <= u < td["u_hi"]:
                             for pos in range(j * UNIT, min(ln, (j + 1) * UNIT)):
-                                pg = pages[page_off + pos // PAGE]
-                                keys.append((pool[pg, 0, :, pos % PAGE], pool[pg, 1, :, pos % PAGE],
-                                             pos if own else -1))
+                                if in_call(x):
+                                    kk, vv = k[x["node_start"] + pos], v[x["node_start"] + pos]
+                                else:
+                                    pg = pages[x["page_off"] + pos // PAGE]
+                                    kk, vv = pool[pg, 0, :, pos % PAGE], pool[pg, 1, :, pos % PAGE]
+                                keys.append((kk, vv, pos if own else -1))
                         u += 1
                 assert td["u_hi"] <= u
                 for tok in range(td["nt"]):
@@ -104,6 +109,16 @@ def emulate(plan, q, k, v, Hq, Hkv, d, schedule="rounds"):
                             out[row, hq], lse[row, hq] = o, l
                         else:
                             parts[(td["part"], row, hq)] = (o, l)
+            for a in apps:  # after the tiles: no tile of the call reads them
+                x = segs[a["seg"]]
+                pg = pages[x["page_off"] + a["page"]]
+                for slot in range(PAGE):
+                    t = a["page"] * PAGE + slot
+                    if t < x["len"]:
+                        pool[pg, 0, :, slot] = k[x["node_start"] + t]
+                        pool[pg, 1, :, slot] = v[x["node_start"] + t]
+                    else:
+                        pool[pg, :, :, slot] = 0.0
             for md in merges[ci["merge_off"]:ci["merge_off"] + ci["n_merges"]]:
                 s = segs[md["seg"]]
                 for tok in range(md["nt"]):
