@@ -110,6 +110,23 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// TMA store of a 3-D box from shared memory, tracked as a bulk group.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int32_t x,
+                                             int32_t y, int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_and_wait_read() {
+  asm volatile(
+      "cp.async.bulk.commit_group;\n\t"
+      "cp.async.bulk.wait_group.read 0;" ::
+          : "memory");
+}
+
 __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar,
                                             int32_t x, int32_t y, int32_t z, int32_t w) {
   asm volatile(
@@ -351,7 +368,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKr,
                    const __grid_constant__ CUtensorMap tmK1, const __grid_constant__ CUtensorMap tmVr,
                    const __grid_constant__ CUtensorMap tmV1, const __grid_constant__ CUtensorMap tmKi,
-                   const __grid_constant__ CUtensorMap tmVi, AttnArgs a) {
+                   const __grid_constant__ CUtensorMap tmVi, const __grid_constant__ CUtensorMap tmO,
+                   AttnArgs a) {
   using C = Cfg<D>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = align1024(smem_raw);
@@ -368,7 +386,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* p_full = s_full + 2;          // [2]: P_h of the current unit is in TMEM
   uint64_t* o_full = p_full + 2;          // [2]: all products of half h done
   uint64_t* first_turn = o_full + 2;      // half A issued its first group
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(first_turn + 1);
+  uint64_t* stage_full = first_turn + 1;  // [2]: half h's output rows are staged in smem
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stage_full + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   // one CTA per (tile, KV head), KV head innermost: blocks start in tile
@@ -402,6 +421,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&o_full[h], 1);
     }
     mbar_init(first_turn, 1);
+    mbar_init(&stage_full[0], 4);
+    mbar_init(&stage_full[1], 4);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -703,10 +724,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int head = hkv * G + (r % G);
       const size_t orow = (size_t)(sd.node_start + token) * a.Hq + head;
       const size_t prow_i = ((size_t)td.part * a.Hkv + hkv) * kRowsPerTile + h * kHalf + r;
+      // A final half whose rows are all tokens of the tile goes out through
+      // the Q_h buffer (its products are done) and TMA stores: rows laid out
+      // like the Q box (token x head), 128-byte swizzled.
+      const bool staged = td.part < 0 && (h + 1) * (kHalf / G) <= td.nt;
+      unsigned char* stage = sQ + h * C::kQHalf;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         float o[32];
         tmem_ld32(trow + o_col + 32 * c, o);
+        if (staged) {
+          unsigned char* rowp = stage + (c >> 1) * C::kQSlab + r * 128;
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 w;
+            w.x = pack_bf16(o[8 * q4 + 0] * inv, o[8 * q4 + 1] * inv);
+            w.y = pack_bf16(o[8 * q4 + 2] * inv, o[8 * q4 + 3] * inv);
+            w.z = pack_bf16(o[8 * q4 + 4] * inv, o[8 * q4 + 5] * inv);
+            w.w = pack_bf16(o[8 * q4 + 6] * inv, o[8 * q4 + 7] * inv);
+            const int chunk = (c & 1) * 4 + q4;
+            *reinterpret_cast<uint4*>(rowp + ((chunk ^ (r & 7)) << 4)) = w;
+          }
+          continue;
+        }
         if (!row_ok) continue;
         if (td.part < 0) {
           uint4* dst = reinterpret_cast<uint4*>(a.out + orow * D + 32 * c);
@@ -725,6 +765,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int q4 = 0; q4 < 8; ++q4)
             dst[q4] = make_float4(o[4 * q4] * inv, o[4 * q4 + 1] * inv, o[4 * q4 + 2] * inv,
                                   o[4 * q4 + 3] * inv);
+        }
+      }
+      if (staged) {
+        fence_proxy_async_smem();  // the TMA (async proxy) reads what this thread wrote
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&stage_full[h]);
+        if ((warp & 3) == 0 && lane == 0) {
+          if (mbar_wait(&stage_full[h], 0, abort_flag)) {
+            for (int slab = 0; slab < D / 64; ++slab)
+              tma_store_3d(&tmO, stage + slab * C::kQSlab, slab * 64, hkv * G,
+                           (int32_t)(sd.node_start + td.t0 + h * (kHalf / G)));
+            bulk_commit_and_wait_read();  // the smem stays valid until the stores read it
+          } else {
+            if (!*abort_flag) raise_error(a.err, kErrTimeout);
+            *abort_flag = 1;
+          }
         }
       }
       if (row_ok) {
@@ -828,7 +884,7 @@ cudaError_t run_call(const AttnLaunch& L) {
   float* part_o = static_cast<float*>(L.workspace);
   float* part_lse = part_o + (size_t)L.n_parts * L.Hkv * kRowsPerTile * D;
   if (L.n_tiles > 0) {
-    CUtensorMap tmQ, tmKr, tmK1, tmVr, tmV1, tmKi, tmVi;
+    CUtensorMap tmQ, tmKr, tmK1, tmVr, tmV1, tmKi, tmVi, tmO;
     {
       // k / v inputs [node_tokens][Hkv][D]: 128 rows of one KV head per box
       cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)L.Hkv, (cuuint64_t)L.node_tokens};
@@ -842,7 +898,8 @@ cudaError_t run_call(const AttnLaunch& L) {
       cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)L.Hq, (cuuint64_t)L.node_tokens};
       cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)L.Hq * D * 2};
       cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)(kHalf / G)};
-      if (!encode(&tmQ, L.q, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      if (!encode(&tmQ, L.q, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+          !encode(&tmO, L.out, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     }
     // pool page: [K: Hkv][16][D] then [V: Hkv][16][D]; dims (inner first)
@@ -891,7 +948,8 @@ cudaError_t run_call(const AttnLaunch& L) {
     cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(attn_tc_kernel<D>), (int)smem);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)L.n_tiles * (unsigned)L.Hkv);
-    attn_tc_kernel<D><<<grid, kThreads, smem, st>>>(tmQ, tmKr, tmK1, tmVr, tmV1, tmKi, tmVi, a);
+    attn_tc_kernel<D><<<grid, kThreads, smem, st>>>(tmQ, tmKr, tmK1, tmVr, tmV1, tmKi, tmVi, tmO,
+                                                    a);
     ++launches;
   }
   if (L.n_merges > 0) {
