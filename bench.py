@@ -3,9 +3,9 @@
 
 A step is one whole pass over one batch of synthetic input: host planning
 (token trie, staged rounds, KV pages, launch lists) and descriptor upload,
-every round's prefix and branch attention (KV append into the paged pool,
-cascade attention, split merges), the fused LM-head readout and the label
-softmax.  The default workload is the yes/no configuration: Hq 32 / Hkv 4 /
+the prefix and branch attention of every staged round (cascade attention
+that also writes the shared segments into the paged pool, split merges), the
+fused LM-head readout and the label softmax.  The default workload is the yes/no configuration: Hq 32 / Hkv 4 /
 d 128, a 2000-token shared prefix with 5 branches of 48 tokens, H 2048,
 V 151936, two labels per branch.
 
@@ -40,8 +40,9 @@ def parse():
     ap.add_argument("--impl", default="libsp", choices=["libsp", "reference"])
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--e2e-steps", type=int, default=50)
-    ap.add_argument("--schedule", default="rounds", choices=["rounds", "all"],
-                    help="attention calls per staged round, or one call for all rounds")
+    ap.add_argument("--schedule", default="all", choices=["rounds", "all"],
+                    help="one prefix and one branch attention call covering every staged "
+                         "round (same work and results), or one pair of calls per round")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the oracle timing (short profiling runs)")
     return ap.parse_args()
@@ -52,6 +53,24 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return ws, rank, local
+
+
+def job_time(local_ms, ws, device=None):
+    """Whole-job time of a replica run: the slowest rank's time (max over
+    ranks; the value every rank returns).  `device` holds the reduction
+    tensor (a CUDA device with NCCL, the CPU with gloo)."""
+    if ws <= 1:
+        return float(local_ms)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(local_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(units_per_rank, ws, ms_per_step):
+    """Aggregate throughput: the units all ranks processed per second."""
+    return units_per_rank * ws / (ms_per_step / 1e3)
 
 
 # --------------------------------------------------------------------------
@@ -234,14 +253,10 @@ def run_libsp(args, ws, rank, local):
     if ws > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
-    total_ms = t_start.elapsed_time(t_stop)
+    total_ms = job_time(t_start.elapsed_time(t_stop), ws, dev)
     attn_ms = [e[0].elapsed_time(e[1]) for e in evs]
     lm_ms = [e[1].elapsed_time(e[2]) for e in evs]
     sm_ms = [e[2].elapsed_time(e[3]) for e in evs]
-    if ws > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
     sp.sp_check_device_error()
 
     # the other attention schedule, same steps, for comparison
@@ -256,7 +271,7 @@ def run_libsp(args, ws, rank, local):
         step(schedule=other)
     o1.record(stream)
     torch.cuda.synchronize()
-    other_ms = o0.elapsed_time(o1) / args.steps
+    other_ms = job_time(o0.elapsed_time(o1), ws, dev) / args.steps
     sp.sp_check_device_error()
 
     # ---- end-to-end through the public call, host buffers --------------------
@@ -295,14 +310,11 @@ def run_libsp(args, ws, rank, local):
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-    if ws > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = job_time(e2e_ms, ws, dev)
     sp.sp_check_device_error()
 
     ms = total_ms / args.steps
-    value = branch_tokens * ws / (ms / 1e3)
+    value = job_value(branch_tokens, ws, ms)
     peaks, peak_kind = load_peaks()
     lm_avg = statistics.mean(lm_ms)
     attn_avg = statistics.mean(attn_ms)
