@@ -40,9 +40,10 @@ def parse():
     ap.add_argument("--impl", default="libsp", choices=["libsp", "reference"])
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--e2e-steps", type=int, default=50)
-    ap.add_argument("--schedule", default="all", choices=["rounds", "all"],
-                    help="one prefix and one branch attention call covering every staged "
-                         "round (same work and results), or one pair of calls per round")
+    ap.add_argument("--schedule", default="tree", choices=["tree", "all", "rounds"],
+                    help="attention calls of a step: one tree call for the whole trie, one "
+                         "prefix and one branch call covering every staged round, or one "
+                         "pair of calls per round (same work and results)")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the oracle timing (short profiling runs)")
     return ap.parse_args()
@@ -259,20 +260,23 @@ def run_libsp(args, ws, rank, local):
     sm_ms = [e[2].elapsed_time(e[3]) for e in evs]
     sp.sp_check_device_error()
 
-    # the other attention schedule, same steps, for comparison
-    other = "all" if args.schedule == "rounds" else "rounds"
-    for _ in range(args.warmup):
-        step(schedule=other)
-    torch.cuda.synchronize()
-    o0 = torch.cuda.Event(enable_timing=True)
-    o1 = torch.cuda.Event(enable_timing=True)
-    o0.record(stream)
-    for i in range(args.steps):
-        step(schedule=other)
-    o1.record(stream)
-    torch.cuda.synchronize()
-    other_ms = job_time(o0.elapsed_time(o1), ws, dev) / args.steps
-    sp.sp_check_device_error()
+    # the other attention schedules, same steps, for comparison
+    others = {}
+    for other in ("tree", "all", "rounds"):
+        if other == args.schedule:
+            continue
+        for _ in range(args.warmup):
+            step(schedule=other)
+        torch.cuda.synchronize()
+        o0 = torch.cuda.Event(enable_timing=True)
+        o1 = torch.cuda.Event(enable_timing=True)
+        o0.record(stream)
+        for i in range(args.steps):
+            step(schedule=other)
+        o1.record(stream)
+        torch.cuda.synchronize()
+        others[other] = job_time(o0.elapsed_time(o1), ws, dev) / args.steps
+        sp.sp_check_device_error()
 
     # ---- end-to-end through the public call, host buffers --------------------
     pin = lambda x: x.pin_memory()
@@ -346,8 +350,9 @@ def run_libsp(args, ws, rank, local):
             "parallelism": f"replicas x{ws} (independent workloads per GPU)",
             "attention_schedule": args.schedule,
         },
-        "other_schedule": {"schedule": other, "ms_per_step": round(other_ms, 5),
-                           "value": round(branch_tokens * ws / (other_ms / 1e3), 1)},
+        "other_schedules": {o: {"ms_per_step": round(t, 5),
+                                "value": round(job_value(branch_tokens, ws, t), 1)}
+                            for o, t in others.items()},
         "decisions_per_s": round(N * ws / (ms / 1e3), 1),
         "logical_tokens_per_s": round(stats["logical_tokens"] * ws / (ms / 1e3), 1),
         "phase_ms": {"attention": round(attn_avg, 5), "label_logprobs": round(lm_avg, 5),

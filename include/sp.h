@@ -147,7 +147,8 @@ sp_status sp_plan_branches(const sp_plan* plan, const int32_t** branch_last_seg,
  * table, ancestor chains, append list, tile list and merge list. */
 sp_status sp_plan_descriptor(const sp_plan* plan, const void** data, size_t* bytes);
 
-/* Launch lists of one call (kind 0 = sp_prefix_attn, 1 = sp_branch_attn) of
+/* Launch lists of one call (kind 0 = sp_prefix_attn, 1 = sp_branch_attn,
+ * 2 = sp_tree_attn) of
  * `round` (or SP_ALL_ROUNDS): info[0..6] = append offset, appends, tile offset, tiles, merge
  * offset, merges (entries of the descriptor lists), partial slots used. */
 sp_status sp_plan_call_info(const sp_plan* plan, int32_t round, int32_t kind, int64_t info[7]);
@@ -164,10 +165,14 @@ sp_status sp_plan_upload(const sp_plan* plan, void* dev_desc, size_t bytes, void
  * sp_prefix_attn handles the shared segments claimed in the round (the
  * article's shared-prefix prefill, computed once); sp_branch_attn handles the
  * branches' own suffixes (the branch prefill against the cached prefix) and
- * recomputed final rows.  Both first append the segments' K/V into the pool,
- * then compute causal softmax attention of every new row over its ancestor
- * segments (read from the pool) and its own segment (causal), scale
- * 1/sqrt(head_dim), and merge the levels with a log-sum-exp combine.
+ * recomputed final rows; sp_tree_attn handles both in one launch.  Each
+ * computes causal softmax attention of every new row over its ancestor
+ * segments and its own segment (causal), scale 1/sqrt(head_dim), the levels
+ * combined with a log-sum-exp merge.  A level computed by the same call is
+ * read from k / v; every other level from the pool, where the call that
+ * computed it wrote it (every call writes the K/V of the shared segments it
+ * computes into their pool pages; leaves are read by no later call and are
+ * not written).
  *
  *   dev_desc  DEVICE, the uploaded descriptor of this plan
  *   round     0 <= round < n_rounds: the segments first computed in that
@@ -194,6 +199,15 @@ sp_status sp_prefix_attn(const sp_plan* plan, const void* dev_desc, int32_t roun
 sp_status sp_branch_attn(const sp_plan* plan, const void* dev_desc, int32_t round, const void* q,
                          const void* k, const void* v, void* kv_pool, void* out, float* lse,
                          void* workspace, size_t ws_bytes, void* stream);
+
+/* sp_prefix_attn and sp_branch_attn of `round` (or SP_ALL_ROUNDS) as one
+ * launch: every segment of the call is read from k / v, so the branches need
+ * not wait for the prefix's pool writes.  With SP_ALL_ROUNDS the whole trie
+ * (the LLM2Jev page's staged rounds included) is one launch whose tiles fill
+ * the GPU without split parts.  Arguments as above. */
+sp_status sp_tree_attn(const sp_plan* plan, const void* dev_desc, int32_t round, const void* q,
+                       const void* k, const void* v, void* kv_pool, void* out, float* lse,
+                       void* workspace, size_t ws_bytes, void* stream);
 
 /* Workspace bytes for sp_label_logprobs with n_branches rows. */
 size_t sp_label_workspace_bytes(int32_t n_branches, int32_t vocab, int32_t n_sms);

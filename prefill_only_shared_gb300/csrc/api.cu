@@ -56,7 +56,7 @@ sp_status attn_call(const sp_plan* P, const void* dev_desc, int32_t round, int k
       (reinterpret_cast<uintptr_t>(dev_desc) & 255u))
     return SP_ERR_ARG;
   const int32_t r = round < 0 ? (int32_t)P->stats.n_rounds : round;
-  const sp_plan::Call& c = P->calls[2 * (size_t)r + kind];
+  const sp_plan::Call& c = P->calls[(size_t)sp_plan::kCallKinds * r + kind];
   const size_t need = (size_t)c.n_parts * P->shape.n_kv_heads * sp::kRowsPerTile *
                       (P->shape.head_dim + 1) * sizeof(float);
   if (need > 0 && (!workspace || ws_bytes < need || !aligned16(workspace)))
@@ -212,6 +212,14 @@ extern "C" sp_status sp_branch_attn(const sp_plan* plan, const void* dev_desc, i
                                     void* out, float* lse, void* workspace, size_t ws_bytes,
                                     void* stream) {
   return attn_call(plan, dev_desc, round, 1, q, k, v, kv_pool, out, lse, workspace, ws_bytes,
+                   stream);
+}
+
+extern "C" sp_status sp_tree_attn(const sp_plan* plan, const void* dev_desc, int32_t round,
+                                    const void* q, const void* k, const void* v, void* kv_pool,
+                                    void* out, float* lse, void* workspace, size_t ws_bytes,
+                                    void* stream) {
+  return attn_call(plan, dev_desc, round, 2, q, k, v, kv_pool, out, lse, workspace, ws_bytes,
                    stream);
 }
 

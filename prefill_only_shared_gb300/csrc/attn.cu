@@ -77,7 +77,7 @@ struct AttnArgs {
   const bf16* v_in;
   bf16* pool;        // [page][K: Hkv x 16 x D | V: Hkv x 16 x D]
   int call_round;    // round of this call, -1 for all rounds
-  int call_kind;     // 0 prefix (shared segments), 1 branch (leaves)
+  int call_kind;     // 0 prefix (shared segments), 1 branch (leaves), 2 both
   bf16* out;
   float* lse;
   float* part_o;
@@ -280,7 +280,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // call writes shared segments into the pool for later calls); every other
 // segment was computed by an earlier call and is read from the pool.
 __device__ __forceinline__ bool computed_here(const AttnArgs& a, const SegDesc& x) {
-  return (x.shared != 0) == (a.call_kind == 0) && (a.call_round < 0 || x.round == a.call_round);
+  const bool kind_ok = a.call_kind == 2 || (x.shared != 0) == (a.call_kind == 0);
+  return kind_ok && (a.call_round < 0 || x.round == a.call_round);
 }
 
 struct Cursor {

@@ -305,21 +305,24 @@ extern "C" sp_status sp_plan_build(const sp_shape* shape, int32_t n_branches,
   std::vector<sp::TileDesc> tiles;
   std::vector<sp::MergeDesc> merges;
   int64_t max_parts = 0;
-  // calls[2 r + kind] for rounds r < n_rounds; calls[2 n_rounds + kind] run the
-  // work of every round in one call.  A call reads the levels it computes
-  // itself from the k / v inputs and every other level from the pool, which
-  // earlier calls have filled, so any grouping of rounds into calls is valid.
-  P->calls.resize(2 * (size_t)n_rounds + 2);
+  // calls[kCallKinds r + kind] for rounds r < n_rounds; calls[kCallKinds
+  // n_rounds + kind] run the work of every round in one call.  Kind 0 holds
+  // the shared segments (prefix call), kind 1 the leaves and the recomputed
+  // final rows (branch call), kind 2 both (tree call).  A call reads the levels
+  // it computes itself from the k / v inputs and every other level from the
+  // pool, which earlier calls have filled, so any grouping of rounds and kinds
+  // into calls is valid.
+  P->calls.resize((size_t)sp_plan::kCallKinds * ((size_t)n_rounds + 1));
   for (int32_t r = 0; r <= n_rounds; ++r) {
     const bool all = r == n_rounds;
-    for (int kind = 0; kind < 2; ++kind) {
-      sp_plan::Call& call = P->calls[2 * r + kind];
+    for (int kind = 0; kind < sp_plan::kCallKinds; ++kind) {
+      sp_plan::Call& call = P->calls[(size_t)sp_plan::kCallKinds * r + kind];
       struct Raw { int32_t seg, t0, nt; int64_t units; };
       std::vector<Raw> raw;
       call.append_off = (int64_t)appends.size();
       for (int32_t s = 0; s < S; ++s) {
         if (!all && P->seg_round[s] != r) continue;
-        if ((kind == 0) != (P->seg_shared[s] != 0)) continue;
+        if (kind < 2 && (kind == 0) != (P->seg_shared[s] != 0)) continue;
         if (P->seg_shared[s])  // leaves are read by no later call
           for (int32_t pg = 0; pg < ceil_div(P->seg_len[s], sp::kPageSize); ++pg)
             appends.push_back({s, pg});
@@ -328,7 +331,7 @@ extern "C" sp_status sp_plan_build(const sp_shape* shape, int32_t n_branches,
           raw.push_back({s, t0, nt, anc_units[s] + ceil_div(t0 + nt, sp::kKeysPerUnit)});
         }
       }
-      if (kind == 1) {
+      if (kind >= 1) {
         const int32_t i0 = all ? 0 : P->round_off[r], i1 = all ? N : P->round_off[r + 1];
         for (int32_t i = i0; i < i1; ++i) {
           int32_t b = all ? i : P->round_branches[i];
@@ -498,10 +501,11 @@ extern "C" sp_status sp_plan_descriptor(const sp_plan* plan, const void** data, 
 
 extern "C" sp_status sp_plan_call_info(const sp_plan* plan, int32_t round, int32_t kind,
                                        int64_t info[7]) {
-  if (!plan || !info || round < -1 || round >= plan->stats.n_rounds || kind < 0 || kind > 1)
+  if (!plan || !info || round < -1 || round >= plan->stats.n_rounds || kind < 0 ||
+      kind >= sp_plan::kCallKinds)
     return SP_ERR_ARG;
   const int32_t r = round < 0 ? (int32_t)plan->stats.n_rounds : round;
-  const sp_plan::Call& c = plan->calls[2 * (size_t)r + kind];
+  const sp_plan::Call& c = plan->calls[(size_t)sp_plan::kCallKinds * r + kind];
   info[0] = c.append_off;
   info[1] = c.n_append;
   info[2] = c.tile_off;

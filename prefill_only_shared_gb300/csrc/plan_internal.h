@@ -24,7 +24,10 @@ struct sp_plan {
   // rounds (CSR)
   std::vector<int32_t> round_off, round_branches;
 
-  // launch lists: calls[2 * round + kind], kind 0 = prefix, 1 = branch
+  // launch lists: calls[kCallKinds * round + kind], kind 0 = prefix (shared
+  // segments), 1 = branch (leaves, recomputed rows), 2 = tree (both); round
+  // n_rounds = every round at once
+  static constexpr int kCallKinds = 3;
   struct Call {
     int64_t append_off = 0, n_append = 0;
     int64_t tile_off = 0, n_tiles = 0;

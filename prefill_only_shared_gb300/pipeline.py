@@ -90,7 +90,8 @@ class SharedPrefixClassifier:
     def attention(self, plan, q, k, v, stream=None, schedule="rounds"):
         """schedule "rounds": one prefix and one branch call per staged round,
         in round order; "all": one prefix call and one branch call covering
-        every round (same results, fewer launches)."""
+        every round; "tree": one call for the whole trie.  Same results,
+        fewer launches."""
         stream = self._stream(stream)
         st = plan.stats()
         T = st["node_tokens"]
@@ -101,12 +102,19 @@ class SharedPrefixClassifier:
         out = self._buf("out", T * Hq * d, torch.bfloat16).view(T, Hq, d)
         lse = self._buf("lse", T * Hq, torch.float32).view(T, Hq)
         launches = 0
-        rounds = range(st["n_rounds"]) if schedule == "rounds" else [sp.SP_ALL_ROUNDS]
-        for r in rounds:
-            sp.sp_prefix_attn(plan, desc, r, q, k, v, self.kv_pool, out, lse, ws, stream)
+        if schedule == "tree":
+            sp.sp_tree_attn(plan, desc, sp.SP_ALL_ROUNDS, q, k, v, self.kv_pool, out, lse, ws,
+                            stream)
             launches += sp.sp_last_launch_count()
-            sp.sp_branch_attn(plan, desc, r, q, k, v, self.kv_pool, out, lse, ws, stream)
-            launches += sp.sp_last_launch_count()
+        else:
+            if schedule not in ("rounds", "all"):
+                raise ValueError(f"unknown schedule {schedule!r}")
+            rounds = range(st["n_rounds"]) if schedule == "rounds" else [sp.SP_ALL_ROUNDS]
+            for r in rounds:
+                sp.sp_prefix_attn(plan, desc, r, q, k, v, self.kv_pool, out, lse, ws, stream)
+                launches += sp.sp_last_launch_count()
+                sp.sp_branch_attn(plan, desc, r, q, k, v, self.kv_pool, out, lse, ws, stream)
+                launches += sp.sp_last_launch_count()
         self.last_attention_launches = launches
         return out, lse
 

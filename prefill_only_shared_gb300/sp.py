@@ -70,6 +70,7 @@ SIGNATURES = {
     "sp_plan_upload": (_I32, [_P, _P, _SZ, _P]),
     "sp_prefix_attn": (_I32, [_P, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "sp_branch_attn": (_I32, [_P, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "sp_tree_attn": (_I32, [_P, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "sp_label_workspace_bytes": (_SZ, [_I32, _I32, _I32]),
     "sp_label_logprobs": (_I32, [_P, _P, _I32, _I32, _I32, _P, _P, _I32, _P, _P, _P, _SZ, _P]),
     "sp_label_logprobs_noalloc": (_I32, [_P, _P, _I32, _I32, _I32, _P, _P, _I32, _P, _P, _P]),
@@ -255,6 +256,11 @@ def sp_prefix_attn(plan, dev_desc, rnd, q, k, v, kv_pool, out, lse, workspace, s
 
 def sp_branch_attn(plan, dev_desc, rnd, q, k, v, kv_pool, out, lse, workspace, stream=None):
     _attn(lib().sp_branch_attn, "sp_branch_attn", plan, dev_desc, rnd, q, k, v, kv_pool, out, lse,
+          workspace, stream)
+
+
+def sp_tree_attn(plan, dev_desc, rnd, q, k, v, kv_pool, out, lse, workspace, stream=None):
+    _attn(lib().sp_tree_attn, "sp_tree_attn", plan, dev_desc, rnd, q, k, v, kv_pool, out, lse,
           workspace, stream)
 
 

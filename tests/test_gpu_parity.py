@@ -43,7 +43,7 @@ SMALL = [
 ]
 
 
-@pytest.mark.parametrize("schedule", ["rounds", "all"])
+@pytest.mark.parametrize("schedule", ["rounds", "all", "tree"])
 @pytest.mark.parametrize("case", range(len(SMALL)))
 def test_small_ragged_cases(cuda_dev, lib, case, schedule):
     trees, Hq, Hkv, d, H, V, labels = SMALL[case]
@@ -75,7 +75,7 @@ def test_recomputed_final_rows(cuda_dev, lib):
     clf = SharedPrefixClassifier(8, 2, 64, 64, 100, device=cuda_dev)
     plan = clf.plan(req, off, toks)
     ro, rl, _ = OA.reference_attention(ref, q, k, v)
-    for schedule in ("rounds", "all"):
+    for schedule in ("rounds", "all", "tree"):
         out, lse = clf.attention(plan, q.cuda(), k.cuda(), v.cuda(), schedule=schedule)
         torch.cuda.synchronize()
         sp.sp_check_device_error()
@@ -83,7 +83,7 @@ def test_recomputed_final_rows(cuda_dev, lib):
         assert np.abs(lse.cpu().numpy() - rl).max() <= TOL_LSE
 
 
-@pytest.mark.parametrize("schedule", ["rounds", "all"])
+@pytest.mark.parametrize("schedule", ["rounds", "all", "tree"])
 @pytest.mark.parametrize("name", ["yesno", "tree2", "choice64"])
 def test_full_size_configs(cuda_dev, lib, name, schedule):
     wl = workload(name)
@@ -96,13 +96,15 @@ def test_full_size_configs(cuda_dev, lib, name, schedule):
     check_readout(wl, g, branches)
 
 
-def test_full_size_batch64(cuda_dev, lib):
+@pytest.mark.parametrize("schedule", ["rounds", "tree"])
+def test_full_size_batch64(cuda_dev, lib, schedule):
     wl = workload("batch64")
-    g = run_gpu(wl)
+    g = run_gpu(wl, schedule=schedule)
     assert len(g["rounds"]) == 2 and len(g["rounds"][0]) == 64
     check_attention_sampled(wl, g, n_random=128)
     check_readout(wl, g, [0, 1, 11, 12, 100, 383, 500, 767])
-    _CACHE.pop("batch64", None)
+    if schedule == "tree":
+        _CACHE.pop("batch64", None)
 
 
 @pytest.mark.parametrize("N,V,H", [(1, 1000, 64), (17, 129, 128), (300, 3000, 136), (1100, 700, 64)])

@@ -51,12 +51,15 @@ def emulate(plan, q, k, v, Hq, Hkv, d, schedule="rounds"):
     lse = np.full((T, Hq), np.nan)
     scale = 1.0 / math.sqrt(d)
     seen = np.zeros(T, dtype=np.int64)
-    for r in (range(st["n_rounds"]) if schedule == "rounds" else [-1]):
-        for kind in (0, 1):
+    per_round = schedule in ("rounds", "tree_rounds")
+    kinds = (2,) if schedule.startswith("tree") else (0, 1)
+    for r in (range(st["n_rounds"]) if per_round else [-1]):
+        for kind in kinds:
             ci = plan.call_info(r, kind)
 
             def in_call(x):
-                return (x["shared"] == 1) == (kind == 0) and (r < 0 or x["round"] == r)
+                kind_ok = kind == 2 or (x["shared"] == 1) == (kind == 0)
+                return kind_ok and (r < 0 or x["round"] == r)
 
             # the call writes exactly its shared segments' pages into the pool
             apps = app[ci["append_off"]:ci["append_off"] + ci["n_append"]]
@@ -137,7 +140,7 @@ def check(req, offs, toks, q, k, v, Hq, Hkv, d, lib, n_sms):
                              n_sms=n_sms)
     ref = S.build_plan(req, offs, toks)
     ro, rl, _ = A.reference_attention(ref, q, k, v)
-    for schedule in ("rounds", "all"):
+    for schedule in ("rounds", "all", "tree", "tree_rounds"):
         out, lse, seen = emulate(plan, q, k, v, Hq, Hkv, d, schedule)
         assert np.abs(out - ro).max() < 1e-10
         assert np.abs(lse - rl).max() < 1e-10
