@@ -30,6 +30,7 @@ constexpr int kKT = 64;          // hidden elements per stage (128 bytes of bf16
 constexpr int kWBytes = kVT * kKT * 2;
 constexpr int kThreads = 192;
 constexpr int kMaxStages = 16;
+constexpr int kLabelCache = 4096;  // label bookkeeping entries kept in shared memory
 constexpr size_t kSmemCap = 227 * 1024;
 
 struct LmArgs {
@@ -39,6 +40,8 @@ struct LmArgs {
   int n_units;  // vocab tiles x chunks
   int stages;
   uint32_t tmem_cols;
+  int n_labels;
+  int lab_cap;  // entries of the shared-memory label branch map and local list
   const int32_t* label_off;
   const int32_t* label_ids;
   float* logits_out;  // raw label logits, [n_labels]; log-probabilities on exit
@@ -64,6 +67,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float2* state = reinterpret_cast<float2*>(tmem_slot + 4);  // [4][N]
+  // labels whose id falls in this CTA's vocab rows (indices into label_ids),
+  // the branch of every label j < lab_cap, and the list length
+  int32_t* lab_list = reinterpret_cast<int32_t*>(state + 4 * a.N);     // [lab_cap]
+  uint16_t* lab_br = reinterpret_cast<uint16_t*>(lab_list + a.lab_cap);  // [lab_cap]
+  int* lab_count = reinterpret_cast<int*>(lab_br + ((a.lab_cap + 1) & ~1));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int u_begin = (int)((int64_t)a.n_units * blockIdx.x / gridDim.x);
@@ -81,6 +89,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
+    *lab_count = 0;
     fence_barrier_init();
     prefetch_tensormap(&tmW);
     prefetch_tensormap(&tmH);
@@ -92,6 +101,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp >= 2) {
     const int q = warp & 3;
     for (int n = lane; n < a.N; n += 32) state[q * a.N + n] = make_float2(-INFINITY, 0.f);
+    // branch of each label j < lab_cap: every thread walks its branches' labels
+    for (int n = threadIdx.x - 64; n < a.N; n += 128) {
+      const int j1 = min(a.label_off[n + 1], a.lab_cap);
+      for (int j = max(a.label_off[n], 0); j < j1; ++j) lab_br[j] = (uint16_t)n;
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -178,6 +192,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- epilogue ----------------
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     float2* st = state + q * a.N;
+    // The labels whose id lies in this CTA's vocab rows, once (the stream is
+    // already filling the pipeline); each tile then checks only those.
+    {
+      const int v_lo = (u_begin / a.n_ch) * kVT;
+      const int v_hi = u_end > u_begin ? ((u_end - 1) / a.n_ch + 1) * kVT : v_lo;
+      for (int j = threadIdx.x - 64; j < a.n_labels; j += 128) {
+        const int id = a.label_ids[j];
+        if (id >= v_lo && id < v_hi) {
+          const int k = atomicAdd(lab_count, 1);
+          if (k < a.lab_cap) lab_list[k] = j;
+        }
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+    }
+    const int n_local = *lab_count;
+    const bool use_list = n_local <= a.lab_cap;
     for (int u = u_begin, i = 0; u < u_end; ++u, ++i) {
       const int b = i & 1;
       const uint32_t use = (uint32_t)(i >> 1);
@@ -214,27 +244,41 @@ __global__ void __launch_bounds__(kThreads, 1)
           st[col0 + lane] = cur;
         }
       }
-      // label logits that fall in this warp's 32 vocab rows
+      // label logits that fall in this warp's 32 vocab rows (from the local
+      // list, or, when it overflowed, from the chunk's whole label range)
       const int n_lo = c * a.nc;
       const int n_hi = min(a.N, n_lo + a.nc);
-      const int j_lo = a.label_off[n_lo], j_hi = a.label_off[n_hi];
+      const int j_lo = use_list ? 0 : a.label_off[n_lo];
+      const int j_hi = use_list ? n_local : a.label_off[n_hi];
       for (int jb = j_lo; jb < j_hi; jb += 32) {
-        const int j = jb + lane;
-        const int id = j < j_hi ? a.label_ids[j] : -1;
-        const bool match = id >= v_base && id < v_base + 32 && id < a.V;
+        const int e = jb + lane;
+        const int j = e < j_hi ? (use_list ? lab_list[e] : e) : -1;
+        const int id = j >= 0 ? a.label_ids[j] : -1;
+        bool match = id >= v_base && id < v_base + 32 && id < a.V;
+        int br = -1;
+        if (match) {
+          // branch of label j: the shared map, else the last n with
+          // label_off[n] <= j (the chunk's range suffices outside list mode)
+          if (j < a.lab_cap) {
+            br = lab_br[j];
+          } else {
+            int lo = use_list ? 0 : n_lo, hi = use_list ? a.N - 1 : n_hi - 1;
+            while (lo < hi) {
+              const int mid = (lo + hi + 1) >> 1;
+              if (a.label_off[mid] <= j) lo = mid; else hi = mid - 1;
+            }
+            br = lo;
+          }
+          match = br >= n_lo && br < n_hi;
+        }
         unsigned bal = __ballot_sync(0xffffffffu, match);
         while (bal) {
           const int src = __ffs(bal) - 1;
           bal &= bal - 1;
           const int jj = __shfl_sync(0xffffffffu, j, src);
           const int idd = __shfl_sync(0xffffffffu, id, src);
-          // branch of label jj: last n in [n_lo, n_hi) with label_off[n] <= jj
-          int lo = n_lo, hi = n_hi - 1;
-          while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (a.label_off[mid] <= jj) lo = mid; else hi = mid - 1;
-          }
-          const float y = tmem_ld1(trow + (uint32_t)(lo - n_lo));
+          const int bb = __shfl_sync(0xffffffffu, br, src);
+          const float y = tmem_ld1(trow + (uint32_t)(bb - n_lo));
           if (lane == idd - v_base) a.logits_out[jj] = y;
         }
       }
@@ -309,12 +353,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 struct Geometry {
-  int nc, n_ch, n_units, grid, stages;
+  int nc, n_ch, n_units, grid, stages, lab_cap;
   size_t smem;
   uint32_t tmem_cols;
 };
 
-Geometry geometry(int N, int V, int n_sms) {
+Geometry geometry(int N, int V, int n_sms, int n_labels = 0) {
   Geometry g{};
   g.n_ch = (N + 255) / 256;
   const int per = (N + g.n_ch - 1) / g.n_ch;
@@ -323,7 +367,18 @@ Geometry geometry(int N, int V, int n_sms) {
   g.n_units = n_vt * g.n_ch;
   g.grid = n_sms < g.n_units ? n_sms : g.n_units;
   const size_t stage = (size_t)kWBytes + (size_t)g.nc * kKT * 2;
-  const size_t fixed = 1024 /*align slack*/ + (2 * kMaxStages + 5) * 8 + 16 + (size_t)4 * N * 8;
+  const size_t base = 1024 /*align slack*/ + (2 * kMaxStages + 5) * 8 + 16 + (size_t)4 * N * 8;
+  // the label cache takes only what is left after min(4, stages that fit
+  // without it) pipeline stages
+  const int st_free = base < kSmemCap ? (int)((kSmemCap - base) / stage) : 0;
+  const int st_keep = st_free < 4 ? st_free : 4;
+  const size_t room = base + (size_t)st_keep * stage < kSmemCap
+                          ? kSmemCap - base - (size_t)st_keep * stage
+                          : 0;
+  int lab = n_labels < kLabelCache ? n_labels : kLabelCache;
+  if ((size_t)lab * 6 + 32 > room) lab = room > 32 ? (int)((room - 32) / 6) : 0;
+  g.lab_cap = lab;
+  const size_t fixed = base + (size_t)g.lab_cap * 6 + 32;
   int st = (int)((kSmemCap - fixed) / stage);
   if (st > kMaxStages) st = kMaxStages;
   g.stages = st;
@@ -352,7 +407,7 @@ size_t lmhead_workspace_bytes(int N, int V, int n_sms) {
 }
 
 cudaError_t lmhead_run(const LmheadLaunch& L) {
-  Geometry g = geometry(L.N, L.V, L.n_sms);
+  Geometry g = geometry(L.N, L.V, L.n_sms, L.n_labels);
   if (g.stages < 2) return cudaErrorInvalidValue;
   CUtensorMap tmW, tmH;
   if (!encode_2d(&tmW, L.W, (uint64_t)L.H, (uint64_t)L.V, kKT, kVT)) return cudaErrorInvalidValue;
@@ -363,6 +418,8 @@ cudaError_t lmhead_run(const LmheadLaunch& L) {
   a.H = L.H;
   a.V = L.V;
   a.nc = g.nc;
+  a.n_labels = L.n_labels;
+  a.lab_cap = g.lab_cap;
   a.n_ch = g.n_ch;
   a.n_units = g.n_units;
   a.stages = g.stages;
