@@ -81,6 +81,7 @@ typedef struct sp_plan_stats {
   int64_t pages_used;
   int64_t desc_bytes;        /* size of the device descriptor (sp_plan_upload)    */
   int64_t attn_workspace_bytes; /* workspace needed by the attention calls      */
+  int64_t cache_hit_tokens;  /* tokens reused from the prefix cache (0 without) */
 } sp_plan_stats;
 
 /* Build a plan from the branches' full token sequences.
@@ -119,6 +120,57 @@ sp_status sp_plan_build(const sp_shape* shape, int32_t n_branches, const int32_t
 
 void sp_plan_free(sp_plan* plan);
 
+/* ---- prefix cache across calls ------------------------------------------
+ *
+ * Source: LLM2Jev "shared prefix" page, section on reusing SGLang's radix
+ * cache (token prefixes whose KV exists are kept across requests, a later
+ * input continues from its first uncached position, and prefixes are evicted
+ * when memory is short; a hot request finds its prefix already cached), and
+ * the openjev-sglang article, section on the repeated state (requests that
+ * repeat a state and change only the questions read only their questions).
+ *
+ * A cache is a host-side radix tree of the shared segments (inner trie nodes)
+ * that earlier plans computed, each owning the pool pages that hold its K/V;
+ * it manages every page of the caller's pool of n_pages pages.  Rules:
+ *  - a branch reuses its longest cached prefix (whole nodes and possibly the
+ *    start of one more), capped one token short of its length: its last
+ *    position is always computed;
+ *  - the uncached remainders are planned and staged like a cold request, in
+ *    groups of the branches of one request whose match ends at the same place;
+ *  - the new shared segments get pool pages (the lowest run of free
+ *    consecutive pages, else the lowest free pages), after evicting unpinned
+ *    cache leaves least recently used first when the free pages do not
+ *    suffice; leaves get no pages (no later call reads them);
+ *  - sp_cache_commit inserts the new shared segments whose group's match ended
+ *    on a node boundary (and whose first token is not taken by a sibling).
+ * Not thread-safe: one thread uses a cache and its plans at a time.  Free
+ * every plan built with a cache before the cache. */
+typedef struct sp_cache sp_cache;
+
+/* A cache over a pool of n_pages >= 1 pages (all free). */
+sp_status sp_cache_create(int32_t n_pages, sp_cache** out);
+void sp_cache_free(sp_cache* cache);
+
+/* out[0..4] = cached segments, cached tokens, pages in use, free pages,
+ * evictions so far. */
+sp_status sp_cache_get_stats(const sp_cache* cache, int64_t out[5]);
+
+/* sp_plan_build with a prefix cache (arguments as there; the pool is the
+ * cache's).  The plan covers only the uncached remainders: node-token rows,
+ * q / k / v / out / lse, exist for the new segments only; cached levels are
+ * read from the pool by the attention calls.  The plan pins the cache nodes
+ * it reads until sp_plan_free.  SP_ERR_POOL_FULL when eviction cannot free
+ * enough pages (nothing changes then except the eviction of unpinned
+ * leaves). */
+sp_status sp_plan_build_cached(const sp_shape* shape, sp_cache* cache, int32_t n_branches,
+                               const int32_t* req_of_branch, const int64_t* tok_offsets,
+                               const int32_t* tokens, int32_t n_sms, sp_plan** out);
+
+/* Insert the plan's new shared segments into the cache.  Call it after the
+ * plan's attention calls are enqueued on the stream that later plans' calls
+ * use (their kernels write the pages).  Committing twice is a no-op. */
+sp_status sp_cache_commit(sp_cache* cache, sp_plan* plan);
+
 sp_status sp_plan_get_stats(const sp_plan* plan, sp_plan_stats* out);
 
 /* Round lists: round r holds round_branches[round_offsets[r] .. round_offsets[r+1]),
@@ -127,12 +179,27 @@ sp_status sp_plan_rounds(const sp_plan* plan, int32_t* n_rounds, const int32_t**
                          const int32_t** round_branches);
 
 /* Segment table (views, length n_segments): request, parent (-1 for a request
- * root), first node-token row, length, round in which it is computed, whether
- * it is shared by >= 2 branches, first KV page. */
+ * root, or with a cache for a root under its group's cached prefix), first
+ * node-token row, length, round in which it is computed, whether it is
+ * shared by >= 2 branches, and the index of its first entry in the
+ * descriptor's page table.  Without a cache the page table is the identity
+ * (segment s owns pool pages first_page, first_page + 1, ...); with a cache
+ * a shared segment's entries name the pool pages the cache gave it and a
+ * leaf's entries are unused placeholders (leaves are never written to the
+ * pool). */
 sp_status sp_plan_segments(const sp_plan* plan, int32_t* n_segments, const int32_t** seg_req,
                            const int32_t** seg_parent, const int64_t** seg_node_start,
                            const int32_t** seg_len, const int32_t** seg_round,
                            const int32_t** seg_shared, const int32_t** seg_first_page);
+
+/* Where each segment's rows come from (views, length n_segments): a branch
+ * that passes through the segment and the position, within that branch's
+ * token sequence, of the segment's first token.  Node-token row
+ * seg_node_start[s] + t holds position seg_pos[s] + t of branch
+ * seg_branch[s]; the caller computes q / k / v of exactly those positions.
+ * With a prefix cache the positions start after the reused tokens. */
+sp_status sp_plan_segment_sources(const sp_plan* plan, const int32_t** seg_branch,
+                                  const int32_t** seg_pos);
 
 /* Per-branch views (length n_branches): segment holding the last token, the
  * node-token row of the last token (the readout position), the branch's

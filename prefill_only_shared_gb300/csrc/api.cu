@@ -82,7 +82,7 @@ sp_status attn_call(const sp_plan* P, const void* dev_desc, int32_t round, int k
   L.Hkv = P->shape.n_kv_heads;
   L.head_dim = P->shape.head_dim;
   L.node_tokens = P->stats.node_tokens;
-  L.pool_pages = P->stats.pages_used;
+  L.pool_pages = P->pool_pages;
   L.err = error_word_ptr();
   if (!L.err) return SP_ERR_CUDA;
   L.stream = stream;

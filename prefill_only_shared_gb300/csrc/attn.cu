@@ -280,6 +280,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // call writes shared segments into the pool for later calls); every other
 // segment was computed by an earlier call and is read from the pool.
 __device__ __forceinline__ bool computed_here(const AttnArgs& a, const SegDesc& x) {
+  if (x.shared == 2) return false;  // a level of the prefix cache: pool only
   const bool kind_ok = a.call_kind == 2 || (x.shared != 0) == (a.call_kind == 0);
   return kind_ok && (a.call_round < 0 || x.round == a.call_round);
 }
@@ -524,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // (warp 8 the K rows, warp 10 the V rows), and the tile holding the
       // segment's last token zero-fills the rest of that page.  No tile of
       // this call reads these pages.
-      if (ok && td.u_lo == 0 && sd.shared && computed_here(a, sd)) {
+      if (ok && td.u_lo == 0 && sd.shared == 1 && computed_here(a, sd)) {
         constexpr int kChunks = D / 8;  // 16-byte chunks per row
         const bf16* src = is_k ? a.k_in : a.v_in;
         const size_t page_elems = (size_t)2 * a.Hkv * kPageSize * D;

@@ -13,8 +13,10 @@ constexpr int kPageSize = 16;      // tokens per KV page
 // the k / v inputs and, once the call that computes it has run and if it is
 // shared, pages page_ids[page_off ..] of the pool; its ancestors (root first)
 // are chain[chain_off .. chain_off + chain_len).  It is computed in round
-// `round`, by the prefix call when `shared` (an inner trie node: at least
-// two branches pass through it), else by the branch call (a leaf).
+// `round`, by the prefix call when `shared` is 1 (an inner trie node: at least
+// two branches pass through it), else by the branch call (a leaf, 0).  Shared
+// 2 marks a level of the prefix cache: computed by an earlier plan, its
+// first `len` keys are read from the pool only.
 struct SegDesc {
   int64_t node_start;  // first node-token row
   int32_t len;

@@ -16,6 +16,7 @@
 #include <cstring>
 #include <map>
 #include <new>
+#include <tuple>
 #include <vector>
 
 #include "plan_internal.h"
@@ -51,10 +52,11 @@ bool shape_ok(const sp_shape& s) {
 
 }  // namespace
 
-extern "C" sp_status sp_plan_build(const sp_shape* shape, int32_t n_branches,
-                                   const int32_t* req_of_branch, const int64_t* tok_offsets,
-                                   const int32_t* tokens, int32_t max_pages, int32_t n_sms,
-                                   sp_plan** out) {
+namespace {
+
+sp_status build(const sp_shape* shape, sp_cache* cache, int32_t n_branches,
+                const int32_t* req_of_branch, const int64_t* tok_offsets, const int32_t* tokens,
+                int32_t max_pages, int32_t n_sms, sp_plan** out) {
   if (!out) return SP_ERR_ARG;
   *out = nullptr;
   if (!shape || !req_of_branch || !tok_offsets || !tokens || n_branches <= 0 || max_pages < 0)
@@ -84,18 +86,71 @@ extern "C" sp_status sp_plan_build(const sp_shape* shape, int32_t n_branches,
   P->max_pages = max_pages;
   P->n_branches = N;
   P->n_requests = (int32_t)by_req.size();
+  P->cache = cache;
+
+  // ---- prefix cache and match groups -------------------------------------
+  // With a cache every branch first reuses its longest cached prefix, capped
+  // one short of its length (the last position is always computed); the
+  // remainders are planned like a cold request, in groups of the branches of
+  // one request whose match ends at the same place (group order: request id,
+  // then smallest branch).  Without a cache a group is a request.
+  std::vector<int64_t> rem_off(N), rem_len(N);
+  std::vector<std::vector<std::pair<int32_t, int32_t>>> bchain(N);
+  int64_t hit_tokens = 0;
+  for (int32_t b = 0; b < N; ++b) {
+    const int64_t off = tok_offsets[b], L = tok_offsets[b + 1] - off;
+    int64_t m = 0;
+    if (cache) {
+      m = sp::cache_match(*cache, tokens + off, L, bchain[b]);
+      if (m > L - 1) {
+        auto& e = bchain[b].back();
+        if (e.second > 1)
+          e.second -= 1;
+        else
+          bchain[b].pop_back();
+        m -= 1;
+      }
+    }
+    rem_off[b] = off + m;
+    rem_len[b] = L - m;
+    hit_tokens += m;
+  }
+  struct Group {
+    int32_t req;
+    std::pair<int32_t, int32_t> end;
+    std::vector<int32_t> members;
+  };
+  std::vector<Group> groups;
+  {
+    std::map<std::tuple<int32_t, int32_t, int32_t>, int32_t> idx;
+    for (int32_t b = 0; b < N; ++b) {
+      const std::pair<int32_t, int32_t> end =
+          bchain[b].empty() ? std::make_pair(0, 0) : bchain[b].back();
+      const auto key = std::make_tuple(req_of_branch[b], end.first, end.second);
+      auto it = idx.find(key);
+      if (it == idx.end()) {
+        idx.emplace(key, (int32_t)groups.size());
+        groups.push_back({req_of_branch[b], end, {b}});
+      } else {
+        groups[it->second].members.push_back(b);
+      }
+    }
+    std::stable_sort(groups.begin(), groups.end(), [](const Group& x, const Group& y) {
+      return x.req != y.req ? x.req < y.req : x.members[0] < y.members[0];
+    });
+  }
 
   // ---- radix trie per request ------------------------------------------
   std::vector<TNode> nodes;
   std::vector<int32_t> roots;  // virtual root per request (len 0)
   std::vector<std::vector<int32_t>> path(N);
-  for (auto& kv : by_req) {
+  for (auto& grp : groups) {
     int32_t root = (int32_t)nodes.size();
     nodes.emplace_back();
     roots.push_back(root);
-    for (int32_t b : kv.second) {
-      const int64_t off = tok_offsets[b];
-      const int64_t L = tok_offsets[b + 1] - off;
+    for (int32_t b : grp.members) {
+      const int64_t off = rem_off[b];
+      const int64_t L = rem_len[b];
       int32_t cur = root;
       int64_t pos = 0;
       while (pos < L) {
@@ -139,9 +194,9 @@ extern "C" sp_status sp_plan_build(const sp_shape* shape, int32_t n_branches,
       }
     }
     // second pass: every branch's path now ends on a node boundary
-    for (int32_t b : kv.second) {
-      const int64_t off = tok_offsets[b];
-      const int64_t L = tok_offsets[b + 1] - off;
+    for (int32_t b : grp.members) {
+      const int64_t off = rem_off[b];
+      const int64_t L = rem_len[b];
       int32_t cur = root;
       int64_t pos = 0;
       while (pos < L) {
@@ -189,34 +244,92 @@ extern "C" sp_status sp_plan_build(const sp_shape* shape, int32_t n_branches,
   P->seg_round.assign(S, -1);
   P->seg_first_page.resize(S);
   P->seg_node_start.resize(S);
+  P->seg_group.resize(S);
+  P->seg_branch.resize(S);
+  P->seg_pos.resize(S);
+  std::vector<int64_t> seg_src(S);
   {
-    // request of each root's subtree
-    std::vector<int32_t> req_of_root_node(nodes.size(), -1);
-    int ri = 0;
-    for (auto& kv : by_req) req_of_root_node[roots[ri++]] = kv.first;
+    // group of each root's subtree
+    std::vector<int32_t> group_of_root_node(nodes.size(), -1);
+    for (size_t g = 0; g < groups.size(); ++g) group_of_root_node[roots[g]] = (int32_t)g;
     int64_t row = 0;
-    int64_t page = 0;
     for (int32_t s = 0; s < S; ++s) {
       const TNode& n = nodes[order[s]];
       P->seg_len[s] = n.len;
-      P->seg_parent[s] = req_of_root_node[n.parent] >= 0 ? -1 : seg_of_node[n.parent];
+      P->seg_parent[s] = group_of_root_node[n.parent] >= 0 ? -1 : seg_of_node[n.parent];
       P->seg_shared[s] = count[s] >= 2 ? 1 : 0;
       P->seg_node_start[s] = row;
-      P->seg_first_page[s] = (int32_t)page;
+      seg_src[s] = n.src;
+      P->seg_branch[s] = n.first_branch;
+      P->seg_pos[s] = (int32_t)(n.src - tok_offsets[n.first_branch]);
       row += n.len;
-      page += ceil_div(n.len, sp::kPageSize);
     }
     for (int32_t s = 0; s < S; ++s) {
       int32_t p = s;
       while (P->seg_parent[p] >= 0) p = P->seg_parent[p];
-      P->seg_req[s] = req_of_root_node[nodes[order[p]].parent];
+      P->seg_group[s] = group_of_root_node[nodes[order[p]].parent];
+      P->seg_req[s] = groups[P->seg_group[s]].req;
     }
     P->stats.node_tokens = row;
+  }
+
+  // ---- KV pages ------------------------------------------------------------
+  // Without a cache every segment owns consecutive pages 0, 1, ... in layout
+  // order.  With a cache only the new shared segments are written to the
+  // pool (leaves are read by no later call): they take pages from the cache,
+  // after evicting least recently used cache leaves when the free pages do not
+  // cover them; a leaf's page-table entries are placeholders (never read).
+  std::vector<int32_t> page_table;
+  if (!cache) {
+    int64_t page = 0;
+    for (int32_t s = 0; s < S; ++s) {
+      P->seg_first_page[s] = (int32_t)page;
+      page += ceil_div(P->seg_len[s], sp::kPageSize);
+    }
     P->stats.pages_used = page;
     if (page > max_pages) {
       delete P;
       return SP_ERR_POOL_FULL;
     }
+    page_table.resize((size_t)page);
+    for (int64_t i = 0; i < page; ++i) page_table[i] = (int32_t)i;
+    P->pool_pages = page;
+  } else {
+    // pin and mark used every node the plan reads
+    for (int32_t b = 0; b < N; ++b)
+      for (auto& e : bchain[b]) P->pinned.push_back(e.first);
+    std::sort(P->pinned.begin(), P->pinned.end());
+    P->pinned.erase(std::unique(P->pinned.begin(), P->pinned.end()), P->pinned.end());
+    for (int32_t nd : P->pinned) {
+      cache->nodes[nd].pins += 1;
+      cache->nodes[nd].last_used = cache->clock;
+    }
+    cache->clock += 1;
+    int64_t need = 0;
+    for (int32_t s = 0; s < S; ++s)
+      if (P->seg_shared[s]) need += ceil_div(P->seg_len[s], sp::kPageSize);
+    while (cache->n_free < need)
+      if (!sp::cache_evict_one(*cache)) {
+        delete P;  // releases the pins
+        return SP_ERR_POOL_FULL;
+      }
+    P->seg_pages.resize(S);
+    P->seg_tokens.resize(S);
+    P->seg_cache_node.assign(S, -1);
+    for (int32_t s = 0; s < S; ++s) {
+      const int32_t np = (int32_t)ceil_div(P->seg_len[s], sp::kPageSize);
+      P->seg_first_page[s] = (int32_t)page_table.size();
+      if (P->seg_shared[s]) {
+        sp::cache_alloc(*cache, np, P->seg_pages[s]);
+        page_table.insert(page_table.end(), P->seg_pages[s].begin(), P->seg_pages[s].end());
+        P->seg_tokens[s].assign(tokens + seg_src[s], tokens + seg_src[s] + P->seg_len[s]);
+      } else {
+        page_table.insert(page_table.end(), (size_t)np, 0);
+      }
+    }
+    P->stats.pages_used = need;
+    P->pool_pages = (int64_t)cache->page_free.size();
+    for (auto& grp : groups) P->group_end.push_back(grp.end);
   }
 
   // ---- staged rounds per request ---------------------------------------
@@ -229,8 +342,8 @@ extern "C" sp_status sp_plan_build(const sp_shape* shape, int32_t n_branches,
     std::vector<char> cached(S, 0);
     std::vector<int32_t> claim_stamp(S, -1);
     int32_t stamp = 0;
-    for (auto& kv : by_req) {
-      std::vector<int32_t> unscored = kv.second;
+    for (auto& grp : groups) {
+      std::vector<int32_t> unscored = grp.members;
       int32_t rnd = 0;
       while (!unscored.empty()) {
         ++stamp;
@@ -278,10 +391,40 @@ extern "C" sp_status sp_plan_build(const sp_shape* shape, int32_t n_branches,
   std::vector<sp::SegDesc> segd(S);
   std::vector<int32_t> chain;
   std::vector<int64_t> anc_units(S, 0);
+  // cached levels: descriptors S, S + 1, ... (K/V in the pool only), one per
+  // (node, visible length) that a group's match passes through
+  std::vector<std::vector<int32_t>> group_levels(groups.size());
+  std::vector<int32_t> level_len;  // visible length per cached level
+  {
+    std::map<std::pair<int32_t, int32_t>, int32_t> level_of;
+    for (size_t g = 0; g < groups.size(); ++g)
+      for (auto& e : bchain[groups[g].members[0]]) {
+        auto it = level_of.find(e);
+        if (it == level_of.end()) {
+          const int32_t id = S + (int32_t)level_len.size();
+          level_of.emplace(e, id);
+          sp::SegDesc d{};
+          d.node_start = 0;
+          d.len = e.second;
+          d.page_off = (int32_t)page_table.size();
+          d.chain_off = 0;
+          d.chain_len = 0;
+          d.round = -1;
+          d.shared = 2;  // cached: read from the pool only
+          const std::vector<int32_t>& pg = cache->nodes[e.first].pages;
+          page_table.insert(page_table.end(), pg.begin(), pg.end());
+          segd.push_back(d);
+          level_len.push_back(e.second);
+          it = level_of.find(e);
+        }
+        group_levels[g].push_back(it->second);
+      }
+  }
   for (int32_t s = 0; s < S; ++s) {
-    std::vector<int32_t> anc;
+    std::vector<int32_t> anc = group_levels[P->seg_group[s]];
+    const size_t n_cached = anc.size();
     for (int32_t p = P->seg_parent[s]; p >= 0; p = P->seg_parent[p]) anc.push_back(p);
-    std::reverse(anc.begin(), anc.end());
+    std::reverse(anc.begin() + (long)n_cached, anc.end());
     segd[s].node_start = P->seg_node_start[s];
     segd[s].len = P->seg_len[s];
     segd[s].page_off = P->seg_first_page[s];
@@ -291,7 +434,8 @@ extern "C" sp_status sp_plan_build(const sp_shape* shape, int32_t n_branches,
     segd[s].shared = P->seg_shared[s] ? 1 : 0;
     for (int32_t a : anc) {
       chain.push_back(a);
-      anc_units[s] += ceil_div(P->seg_len[a], sp::kKeysPerUnit);
+      const int32_t alen = a < S ? P->seg_len[a] : level_len[a - S];
+      anc_units[s] += ceil_div(alen, sp::kKeysPerUnit);
     }
   }
 
@@ -393,13 +537,13 @@ extern "C" sp_status sp_plan_build(const sp_shape* shape, int32_t n_branches,
   sp::DescHeader h{};
   size_t off = align256(sizeof(sp::DescHeader));
   h.off_segs = (int64_t)off;    off = align256(off + segd.size() * sizeof(sp::SegDesc));
-  h.off_pages = (int64_t)off;   off = align256(off + (size_t)P->stats.pages_used * sizeof(int32_t));
+  h.off_pages = (int64_t)off;   off = align256(off + page_table.size() * sizeof(int32_t));
   h.off_chain = (int64_t)off;   off = align256(off + chain.size() * sizeof(int32_t));
   h.off_append = (int64_t)off;  off = align256(off + appends.size() * sizeof(sp::AppendDesc));
   h.off_tiles = (int64_t)off;   off = align256(off + tiles.size() * sizeof(sp::TileDesc));
   h.off_merges = (int64_t)off;  off = align256(off + merges.size() * sizeof(sp::MergeDesc));
-  h.n_segs = S;
-  h.n_pages = P->stats.pages_used;
+  h.n_segs = (int64_t)segd.size();
+  h.n_pages = (int64_t)page_table.size();
   h.n_chain = (int64_t)chain.size();
   h.n_append = (int64_t)appends.size();
   h.n_tiles = (int64_t)tiles.size();
@@ -407,10 +551,8 @@ extern "C" sp_status sp_plan_build(const sp_shape* shape, int32_t n_branches,
   P->blob.assign(off, 0);
   std::memcpy(P->blob.data(), &h, sizeof(h));
   if (!segd.empty()) std::memcpy(P->blob.data() + h.off_segs, segd.data(), segd.size() * sizeof(sp::SegDesc));
-  {
-    int32_t* pg = reinterpret_cast<int32_t*>(P->blob.data() + h.off_pages);
-    for (int64_t i = 0; i < P->stats.pages_used; ++i) pg[i] = (int32_t)i;
-  }
+  if (!page_table.empty())
+    std::memcpy(P->blob.data() + h.off_pages, page_table.data(), page_table.size() * sizeof(int32_t));
   if (!chain.empty()) std::memcpy(P->blob.data() + h.off_chain, chain.data(), chain.size() * sizeof(int32_t));
   if (!appends.empty()) std::memcpy(P->blob.data() + h.off_append, appends.data(), appends.size() * sizeof(sp::AppendDesc));
   if (!tiles.empty()) std::memcpy(P->blob.data() + h.off_tiles, tiles.data(), tiles.size() * sizeof(sp::TileDesc));
@@ -433,6 +575,7 @@ extern "C" sp_status sp_plan_build(const sp_shape* shape, int32_t n_branches,
   P->stats.logical_tokens = logical;
   P->stats.computed_tokens = P->stats.node_tokens + recomputed;
   P->stats.reused_tokens = logical - P->stats.computed_tokens;
+  P->stats.cache_hit_tokens = hit_tokens;
   P->stats.desc_bytes = (int64_t)P->blob.size();
   // partial O and lse per split part
   P->stats.attn_workspace_bytes = (int64_t)align256(
@@ -440,6 +583,27 @@ extern "C" sp_status sp_plan_build(const sp_shape* shape, int32_t n_branches,
       sizeof(float));
   *out = P;
   return SP_OK;
+}
+
+}  // namespace
+
+extern "C" sp_status sp_plan_build(const sp_shape* shape, int32_t n_branches,
+                                   const int32_t* req_of_branch, const int64_t* tok_offsets,
+                                   const int32_t* tokens, int32_t max_pages, int32_t n_sms,
+                                   sp_plan** out) {
+  return build(shape, nullptr, n_branches, req_of_branch, tok_offsets, tokens, max_pages, n_sms,
+               out);
+}
+
+extern "C" sp_status sp_plan_build_cached(const sp_shape* shape, sp_cache* cache,
+                                          int32_t n_branches, const int32_t* req_of_branch,
+                                          const int64_t* tok_offsets, const int32_t* tokens,
+                                          int32_t n_sms, sp_plan** out) {
+  if (!cache) {
+    if (out) *out = nullptr;
+    return SP_ERR_ARG;
+  }
+  return build(shape, cache, n_branches, req_of_branch, tok_offsets, tokens, 0, n_sms, out);
 }
 
 extern "C" void sp_plan_free(sp_plan* plan) { delete plan; }
@@ -476,6 +640,14 @@ extern "C" sp_status sp_plan_segments(const sp_plan* plan, int32_t* n_segments,
   *seg_round = plan->seg_round.data();
   *seg_shared = plan->seg_shared.data();
   *seg_first_page = plan->seg_first_page.data();
+  return SP_OK;
+}
+
+extern "C" sp_status sp_plan_segment_sources(const sp_plan* plan, const int32_t** seg_branch,
+                                             const int32_t** seg_pos) {
+  if (!plan || !seg_branch || !seg_pos) return SP_ERR_ARG;
+  *seg_branch = plan->seg_branch.data();
+  *seg_pos = plan->seg_pos.data();
   return SP_OK;
 }
 

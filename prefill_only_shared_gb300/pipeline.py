@@ -32,11 +32,22 @@ class PassOutputs:
 
 class SharedPrefixClassifier:
     def __init__(self, n_q_heads, n_kv_heads, head_dim, hidden, vocab, max_pages=None,
-                 device="cuda:0", page_size=16):
+                 device="cuda:0", page_size=16, prefix_cache_pages=None):
         """``max_pages``: fixed KV pool capacity (plans that need more fail
-        with SP_ERR_POOL_FULL); None grows the pool to what each plan needs."""
+        with SP_ERR_POOL_FULL); None grows the pool to what each plan needs.
+
+        ``prefix_cache_pages``: keep the shared segments that calls compute in
+        a radix cache over a fixed pool of that many pages (it replaces
+        ``max_pages``), so later calls compute only their uncached remainders
+        (repeated state, hot requests).  A plan is then committed to the cache
+        when its attention is enqueued; all calls must use one stream, since
+        pages freed by one plan are written by the next."""
         self.shape = sp.make_shape(n_q_heads, n_kv_heads, head_dim, page_size, hidden, vocab)
         self.device = torch.device(device)
+        self.cache = None
+        if prefix_cache_pages is not None:
+            self.cache = sp.Cache(int(prefix_cache_pages))
+            max_pages = int(prefix_cache_pages)
         self.fixed_pool = max_pages is not None
         self.n_sms = torch.cuda.get_device_properties(self.device).multi_processor_count
         self._bufs = {}
@@ -82,6 +93,11 @@ class SharedPrefixClassifier:
         return int(stream)
 
     def plan(self, req_of_branch, tok_offsets, tokens) -> "sp.Plan":
+        """The plan of one call.  With a prefix cache it covers only the
+        uncached remainders: q / k / v rows exist for those alone."""
+        if self.cache is not None:
+            return sp.sp_plan_build_cached(self.shape, self.cache, req_of_branch, tok_offsets,
+                                           tokens, self.n_sms)
         plan = sp.sp_plan_build(self.shape, req_of_branch, tok_offsets, tokens, self.max_pages,
                                 self.n_sms)
         self._ensure_pool(plan.stats()["pages_used"])
@@ -116,6 +132,8 @@ class SharedPrefixClassifier:
                 sp.sp_branch_attn(plan, desc, r, q, k, v, self.kv_pool, out, lse, ws, stream)
                 launches += sp.sp_last_launch_count()
         self.last_attention_launches = launches
+        if plan.cache is not None:  # later plans on this stream may read its segments
+            sp.sp_cache_commit(plan.cache, plan)
         return out, lse
 
     def _desc_view(self, nbytes):

@@ -42,7 +42,7 @@ class sp_plan_stats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in (
         "n_requests", "n_branches", "n_segments", "n_shared_segments", "n_rounds",
         "logical_tokens", "computed_tokens", "reused_tokens", "node_tokens", "pages_used",
-        "desc_bytes", "attn_workspace_bytes")]
+        "desc_bytes", "attn_workspace_bytes", "cache_hit_tokens")]
 
     def as_dict(self):
         return {n: int(getattr(self, n)) for n, _ in self._fields_}
@@ -59,10 +59,17 @@ SIGNATURES = {
     "sp_plan_build": (_I32, [ctypes.POINTER(sp_shape), _I32, _I32P, _I64P, _I32P, _I32, _I32,
                              ctypes.POINTER(_P)]),
     "sp_plan_free": (None, [_P]),
+    "sp_cache_create": (_I32, [_I32, ctypes.POINTER(_P)]),
+    "sp_cache_free": (None, [_P]),
+    "sp_cache_get_stats": (_I32, [_P, _I64P]),
+    "sp_plan_build_cached": (_I32, [ctypes.POINTER(sp_shape), _P, _I32, _I32P, _I64P, _I32P, _I32,
+                                    ctypes.POINTER(_P)]),
+    "sp_cache_commit": (_I32, [_P, _P]),
     "sp_plan_get_stats": (_I32, [_P, ctypes.POINTER(sp_plan_stats)]),
     "sp_plan_rounds": (_I32, [_P, _I32P, ctypes.POINTER(_I32P), ctypes.POINTER(_I32P)]),
     "sp_plan_segments": (_I32, [_P, _I32P] + [ctypes.POINTER(_I32P)] * 2 + [ctypes.POINTER(_I64P)]
                          + [ctypes.POINTER(_I32P)] * 4),
+    "sp_plan_segment_sources": (_I32, [_P, ctypes.POINTER(_I32P), ctypes.POINTER(_I32P)]),
     "sp_plan_branches": (_I32, [_P, ctypes.POINTER(_I32P), ctypes.POINTER(_I64P),
                                 ctypes.POINTER(_I32P), ctypes.POINTER(_I32P)]),
     "sp_plan_descriptor": (_I32, [_P, ctypes.POINTER(_P), ctypes.POINTER(_SZ)]),
@@ -144,12 +151,14 @@ def _np(a, dtype):
 
 
 class Plan:
-    """Owns an sp_plan*; host-only."""
+    """Owns an sp_plan*; host-only.  A plan built with a prefix cache keeps the
+    cache alive (the plan must be freed first)."""
 
-    def __init__(self, ptr: ctypes.c_void_p, shape: sp_shape):
+    def __init__(self, ptr: ctypes.c_void_p, shape: sp_shape, cache=None):
         self._ptr = ptr
         self.shape = shape
         self._stats = None
+        self.cache = cache
 
     @property
     def ptr(self):
@@ -207,12 +216,63 @@ class Plan:
         keys = ["append_off", "n_append", "tile_off", "n_tiles", "merge_off", "n_merges", "n_parts"]
         return {k: int(x) for k, x in zip(keys, info)}
 
+    def segment_sources(self) -> dict:
+        """Per segment: a branch through it and its first token's position in
+        that branch."""
+        n = self.stats()["n_segments"]
+        ptrs = [_I32P(), _I32P()]
+        _check(lib().sp_plan_segment_sources(self._ptr, *[ctypes.byref(p) for p in ptrs]),
+               "sp_plan_segment_sources")
+        return {k: np.ctypeslib.as_array(p, shape=(n,)).copy() if n else np.zeros(0, np.int32)
+                for k, p in zip(("branch", "pos"), ptrs)}
+
+    def row_sources(self):
+        """(branch, position) of every node-token row, int64 arrays."""
+        seg, src = self.segments(), self.segment_sources()
+        lens = seg["len"].astype(np.int64)
+        rows_b = np.repeat(src["branch"].astype(np.int64), lens)
+        start = np.repeat(seg["node_start"].astype(np.int64), lens)
+        pos0 = np.repeat(src["pos"].astype(np.int64), lens)
+        r = np.arange(int(lens.sum()), dtype=np.int64)  # segments are in row order
+        return rows_b, pos0 + (r - start)
+
     def branches(self) -> dict:
         nb = self.stats()["n_branches"]
         ptrs = [_I32P(), _I64P(), _I32P(), _I32P()]
         _check(lib().sp_plan_branches(self._ptr, *[ctypes.byref(p) for p in ptrs]), "sp_plan_branches")
         names = ["last_seg", "last_row", "round", "recompute"]
         return {k: np.ctypeslib.as_array(p, shape=(nb,)).copy() for k, p in zip(names, ptrs)}
+
+
+class Cache:
+    """Owns an sp_cache*: the radix cache of shared segments over a KV pool of
+    n_pages pages, kept across calls.  Host-only; one thread at a time."""
+
+    STAT_NAMES = ("segments", "tokens", "pages_used", "pages_free", "evictions")
+
+    def __init__(self, n_pages: int):
+        self._ptr = None
+        out = ctypes.c_void_p()
+        _check(lib().sp_cache_create(int(n_pages), ctypes.byref(out)), "sp_cache_create")
+        self._ptr = out
+        self.n_pages = int(n_pages)
+
+    @property
+    def ptr(self):
+        return self._ptr
+
+    def stats(self) -> dict:
+        out = (ctypes.c_int64 * 5)()
+        _check(lib().sp_cache_get_stats(self._ptr, out), "sp_cache_get_stats")
+        return {k: int(x) for k, x in zip(self.STAT_NAMES, out)}
+
+    def __del__(self):
+        try:
+            if self._ptr:
+                lib().sp_cache_free(self._ptr)
+                self._ptr = None
+        except Exception:
+            pass
 
 
 def make_shape(n_q_heads, n_kv_heads, head_dim, page_size, hidden, vocab) -> sp_shape:
@@ -232,6 +292,25 @@ def sp_plan_build(shape: sp_shape, req_of_branch, tok_offsets, tokens, max_pages
                              int(n_sms), ctypes.byref(out))
     _check(st, "sp_plan_build")
     return Plan(out, shape)
+
+
+def sp_plan_build_cached(shape: sp_shape, cache: Cache, req_of_branch, tok_offsets, tokens,
+                         n_sms: int = 0) -> Plan:
+    req = _np(req_of_branch, np.int32)
+    off = _np(tok_offsets, np.int64)
+    tok = _np(tokens, np.int32)
+    if len(off) != len(req) + 1:
+        raise ValueError("tok_offsets must have n_branches + 1 entries")
+    out = ctypes.c_void_p()
+    st = lib().sp_plan_build_cached(ctypes.byref(shape), cache.ptr, len(req),
+                                    req.ctypes.data_as(_I32P), off.ctypes.data_as(_I64P),
+                                    tok.ctypes.data_as(_I32P), int(n_sms), ctypes.byref(out))
+    _check(st, "sp_plan_build_cached")
+    return Plan(out, shape, cache)
+
+
+def sp_cache_commit(cache: Cache, plan: Plan):
+    _check(lib().sp_cache_commit(cache.ptr, plan.ptr), "sp_cache_commit")
 
 
 def sp_plan_upload(plan: Plan, dev_desc: torch.Tensor, stream=None):

@@ -41,11 +41,15 @@ def decode(blob):
             arr("tiles", TILE), arr("merges", MERGE))
 
 
-def emulate(plan, q, k, v, Hq, Hkv, d, schedule="rounds"):
+def emulate(plan, q, k, v, Hq, Hkv, d, schedule="rounds", pool=None):
+    """pool: a persistent (pages, 2, Hkv, PAGE, d) array for plans built with a
+    prefix cache (cached levels are read from it, new shared segments written
+    to it); None = a fresh NaN pool."""
     segs, pages, chain, app, tiles, merges = decode(plan.descriptor())
     st = plan.stats()
     G = Hq // Hkv
-    pool = np.full((max(st["pages_used"], 1), 2, Hkv, PAGE, d), np.nan)
+    if pool is None:
+        pool = np.full((max(st["pages_used"], 1), 2, Hkv, PAGE, d), np.nan)
     T = st["node_tokens"]
     out = np.full((T, Hq, d), np.nan)
     lse = np.full((T, Hq), np.nan)
@@ -58,12 +62,14 @@ def emulate(plan, q, k, v, Hq, Hkv, d, schedule="rounds"):
             ci = plan.call_info(r, kind)
 
             def in_call(x):
+                if x["shared"] == 2:  # a cached level: K/V only in the pool
+                    return False
                 kind_ok = kind == 2 or (x["shared"] == 1) == (kind == 0)
                 return kind_ok and (r < 0 or x["round"] == r)
 
             # the call writes exactly its shared segments' pages into the pool
             apps = app[ci["append_off"]:ci["append_off"] + ci["n_append"]]
-            want = sorted((i, p) for i, x in enumerate(segs) if in_call(x) and x["shared"]
+            want = sorted((i, p) for i, x in enumerate(segs) if in_call(x) and x["shared"] == 1
                           for p in range((x["len"] + PAGE - 1) // PAGE))
             assert sorted((int(a["seg"]), int(a["page"])) for a in apps) == want
             parts = {}
