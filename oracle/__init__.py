@@ -22,6 +22,11 @@ Everything is computed from the plain definition, in float64 with numpy:
 * ``postprocess``   -- question-type readouts and the confidence value
                        (same article, sections on confidence and on the three
                        question types).
+* ``cache``         -- the radix prefix cache across calls (LLM2Jev page,
+                       section on reusing the radix cache).
+* ``options``       -- multi-token option scores (chain-rule sums of
+                       readout log-probabilities) and label-prior calibration
+                       (openjev-multimodal performance page, next steps).
 
 Parity status of every function is stated in its module docstring; all are
 pinned by tests under ``tests/`` marked ``not gpu``.
