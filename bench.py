@@ -320,6 +320,31 @@ def run_libsp(args, ws, rank, local):
     warm_launches = cclf.last_launches
     del cclf
 
+    # ---- multi-token options with a calibration prior ---------------------------
+    # (the readout at every option token -- one label per row -- then the option
+    # scores and their calibrated softmax per question; the LM head is the one
+    # above, model state)
+    from prefill_only_shared_gb300.workloads import make_options
+    owl = make_options(seed=0, hidden=sh.hidden, vocab=sh.vocab, with_W=False)
+    o_h = owl.h_rows.to(dev)
+    o_off = torch.from_numpy(owl.opt_off).to(dev)
+    o_tok = torch.from_numpy(owl.tokens).to(dev)
+    o_q = torch.from_numpy(owl.q_off).to(dev)
+    o_prior = torch.from_numpy(owl.prior).to(dev)
+    for _ in range(args.warmup):
+        clf.options(o_h, W, o_off, o_tok, o_q, o_prior, stream)
+    torch.cuda.synchronize()
+    oev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        oev[i][0].record(stream)
+        clf.options(o_h, W, o_off, o_tok, o_q, o_prior, stream)
+        oev[i][1].record(stream)
+    torch.cuda.synchronize()
+    sp.sp_check_device_error()
+    opt_ms = job_time(statistics.mean(e[0].elapsed_time(e[1]) for e in oev), ws, dev)
+    opt_bytes = sh.vocab * sh.hidden * 2 + owl.n_rows * sh.hidden * 2 + owl.n_rows * 8
+    opt_launches = clf.last_option_launches
+
     # ---- end-to-end through the public call, host buffers --------------------
     pin = lambda x: x.pin_memory()
     hq, hk, hv, hh = pin(wl.q), pin(wl.k), pin(wl.v), pin(wl.h)
@@ -414,6 +439,22 @@ def run_libsp(args, ws, rank, local):
             "computed_tokens": int(warm_stats["computed_tokens"]),
             "cache_hit_tokens": int(warm_stats["cache_hit_tokens"]),
             "gpu_launches_per_step": int(warm_launches),
+        },
+        "options": {
+            "workload": f"{owl.n_questions} questions of 2..8 options of 1..4 tokens "
+                        f"({owl.n_opts} options, {owl.n_rows} option tokens), each token read out "
+                        f"at the position before it, calibrated by a per-option prior; "
+                        f"H {sh.hidden}, V {sh.vocab}",
+            "ms_per_call": round(opt_ms, 5),
+            "decisions_per_s": round(owl.n_questions * ws / (opt_ms / 1e3), 1),
+            "roofline": {"bound": "hbm",
+                         "achieved": round(opt_bytes / (opt_ms / 1e3) / 1e9, 1),
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(opt_bytes / (opt_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+                         "algorithmic_bytes_per_call": opt_bytes,
+                         "note": "sp_label_logprobs over the option-token rows plus "
+                                 "sp_option_softmax, timed together"},
+            "gpu_launches_per_call": int(opt_launches),
         },
         "decisions_per_s": round(N * ws / (ms / 1e3), 1),
         "logical_tokens_per_s": round(stats["logical_tokens"] * ws / (ms / 1e3), 1),

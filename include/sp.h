@@ -403,6 +403,48 @@ sp_status sp_candidate_decide(const float* probs, const int32_t* label_off, int3
                               float* dist, int32_t* argmax, float* value, float* confidence,
                               void* stream);
 
+/* Multi-token option scoring with optional label-prior calibration
+ * (openjev-multimodal "performance" page, section on next steps, which
+ * names both as planned work that changes the probabilities; the pages give
+ * no formula, so this is the library's reading):
+ *
+ *   scores[o]  = sum of row_logprobs[r], r = opt_off[o] .. opt_off[o+1]-1:
+ *                the option's joint log-probability by the chain rule, its
+ *                rows being the log-probability of each option token at the
+ *                position before it (sp_label_logprobs with one label per
+ *                row: the last prompt position for the first token, the
+ *                previous option token's position for the others)
+ *   probs[o]   = exp(x_o - m) / sum_i exp(x_i - m) over the options of o's
+ *                question, x_o = scores[o] - prior[o] (prior NULL: 0), m the
+ *                question's maximum; the prior is a per-option log-probability
+ *                such as the same readout on a content-free input (the
+ *                diagonal form of contextual calibration)
+ *   argmax[q]  = index within question q of the largest x; lowest on ties
+ *
+ * A one-token option without a prior is exactly the label softmax.
+ *   row_logprobs  DEVICE fp32 [n_rows]
+ *   opt_off       DEVICE int32 [n_opts+1]: option o owns rows opt_off[o] .. opt_off[o+1]-1
+ *   q_off         DEVICE int32 [n_questions+1]: question q owns options
+ *                 q_off[q] .. q_off[q+1]-1; q_off[n_questions] <= n_opts
+ *   prior         DEVICE fp32 [n_opts] or NULL
+ *   scores, probs DEVICE fp32 [n_opts];  argmax: DEVICE int32 [n_questions]
+ * Device-side checks: a question with an option count outside 2..64, an
+ * option with no rows or with rows outside [0, n_rows), or options past
+ * n_opts give NaN / -1 outputs for that question and raise
+ * SP_ERR_DEVICE_BOUNDS.  One launch, one warp per question.  SP_ERR_ARG for
+ * null pointers (other than prior) or n_rows < 1, n_opts < 2, n_questions < 1. */
+sp_status sp_option_softmax(const float* row_logprobs, int32_t n_rows, const int32_t* opt_off,
+                            int32_t n_opts, const int32_t* q_off, int32_t n_questions,
+                            const float* prior, float* scores, float* probs, int32_t* argmax,
+                            void* stream);
+
+/* Host-side validation of the option CSRs of sp_option_softmax (HOST
+ * arrays): opt_off starts at 0, increases strictly and ends <= n_rows; q_off
+ * starts at 0, ends <= n_opts, and gives every question 2..64 options.
+ * SP_OK or SP_ERR_ARG. */
+sp_status sp_check_options(const int32_t* opt_off, int32_t n_opts, int32_t n_rows,
+                           const int32_t* q_off, int32_t n_questions);
+
 /* Host-side validation of a label CSR (HOST arrays): counts in [2, 64],
  * 0 <= id < vocab, monotone offsets.  SP_OK or SP_ERR_ARG. */
 sp_status sp_check_labels(const int32_t* label_off, const int32_t* label_ids, int32_t N,

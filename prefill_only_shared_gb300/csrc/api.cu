@@ -344,6 +344,23 @@ extern "C" sp_status sp_candidate_decide(const float* probs, const int32_t* labe
   return e == cudaSuccess ? SP_OK : SP_ERR_CUDA;
 }
 
+extern "C" sp_status sp_option_softmax(const float* row_logprobs, int32_t n_rows,
+                                       const int32_t* opt_off, int32_t n_opts,
+                                       const int32_t* q_off, int32_t n_questions,
+                                       const float* prior, float* scores, float* probs,
+                                       int32_t* argmax, void* stream) {
+  t_last_launches = 0;
+  if (!row_logprobs || !opt_off || !q_off || !scores || !probs || !argmax || n_rows < 1 ||
+      n_opts < 2 || n_questions < 1)
+    return SP_ERR_ARG;
+  unsigned* err = error_word_ptr();
+  if (!err) return SP_ERR_CUDA;
+  cudaError_t e = sp::option_softmax_run(row_logprobs, n_rows, opt_off, n_opts, q_off,
+                                         n_questions, prior, scores, probs, argmax, err, stream);
+  t_last_launches = 1;
+  return e == cudaSuccess ? SP_OK : SP_ERR_CUDA;
+}
+
 extern "C" sp_status sp_wait_flag(const uint32_t* flag, uint32_t expect, int64_t limit_ns,
                                   void* stream) {
   t_last_launches = 0;

@@ -10,6 +10,11 @@
 //   outputs: every choice option and score level is its own yes/no input and
 //   the final answers are read after normalisation.
 //
+// * openjev-multimodal "performance" page, section on next steps: multi-token
+//   option scoring and label-prior calibration (read as the chain-rule sum of
+//   the option tokens' log-probabilities, minus an optional prior, then the
+//   stable softmax over the question's options).
+//
 // One warp per branch (or per question), at most 64 options: two per lane.
 #include "../../include/sp.h"
 #include "common.cuh"
@@ -169,7 +174,79 @@ __global__ void __launch_bounds__(128) candidate_decide_kernel(
   }
 }
 
+// Option scores and their calibrated softmax, one warp per question.  Lane l
+// sums the rows of options l and l + 32 of the question (their token
+// log-probabilities, in token order), subtracts the option's prior, and the
+// warp takes the stable softmax and the lowest-index argmax.
+__global__ void __launch_bounds__(128) option_softmax_kernel(
+    const float* row_lp, int n_rows, const int32_t* opt_off, int n_opts, const int32_t* q_off,
+    int Q, const float* prior, float* scores, float* probs, int32_t* argmax, unsigned* err) {
+  const int q = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (q >= Q) return;
+  const int a = q_off[q], b = q_off[q + 1], total = q_off[Q];
+  const int K = b - a;
+  // The question's options lie inside [0, total) and total <= n_opts: every
+  // opt_off / prior / scores / probs index below is then in bounds.
+  const bool range_ok = a >= 0 && K >= 0 && b <= total && total <= n_opts;
+  bool bad = !range_ok || K < 2 || K > 64;
+  float sc[2] = {0.f, 0.f}, x[2] = {-INFINITY, -INFINITY};
+  if (!bad) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int j = lane + 32 * i;
+      if (j >= K) continue;
+      const int o = a + j;
+      const int r0 = opt_off[o], r1 = opt_off[o + 1];
+      if (r0 < 0 || r1 <= r0 || r1 > n_rows) {  // an empty option or rows out of range
+        bad = true;
+        continue;
+      }
+      float t = 0.f;
+      for (int r = r0; r < r1; ++r) t += row_lp[r];
+      sc[i] = t;
+      x[i] = prior ? t - prior[o] : t;
+    }
+  }
+  if (__any_sync(kFull, bad)) {
+    if (range_ok)
+      for (int j = lane; j < K; j += 32) {
+        scores[a + j] = qnan();
+        probs[a + j] = qnan();
+      }
+    if (lane == 0) {
+      argmax[q] = -1;
+      raise_error(err, kErrBounds);
+    }
+    return;
+  }
+  float m;
+  int bi;
+  warp_argmax(x[0], x[1], lane, m, bi);
+  const float e0 = lane < K ? __expf(x[0] - m) : 0.f;
+  const float e1 = lane + 32 < K ? __expf(x[1] - m) : 0.f;
+  const float inv = 1.f / warp_sum(e0 + e1);
+  if (lane < K) {
+    scores[a + lane] = sc[0];
+    probs[a + lane] = e0 * inv;
+  }
+  if (lane + 32 < K) {
+    scores[a + lane + 32] = sc[1];
+    probs[a + lane + 32] = e1 * inv;
+  }
+  if (lane == 0) argmax[q] = bi;
+}
+
 }  // namespace
+
+cudaError_t option_softmax_run(const float* row_lp, int n_rows, const int32_t* opt_off,
+                               int n_opts, const int32_t* q_off, int Q, const float* prior,
+                               float* scores, float* probs, int32_t* argmax, unsigned* err,
+                               void* stream) {
+  option_softmax_kernel<<<(Q + 3) / 4, 128, 0, static_cast<cudaStream_t>(stream)>>>(
+      row_lp, n_rows, opt_off, n_opts, q_off, Q, prior, scores, probs, argmax, err);
+  return cudaGetLastError();
+}
 
 cudaError_t label_softmax_run(const float* logprobs, const int32_t* label_off, int N, float* probs,
                               int32_t* argmax, unsigned* err, void* stream) {

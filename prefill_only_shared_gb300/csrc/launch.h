@@ -70,6 +70,11 @@ cudaError_t candidate_decide_run(const float* probs, const int32_t* label_off, i
                                  int32_t* argmax, float* value, float* conf, unsigned* err,
                                  void* stream);
 
+cudaError_t option_softmax_run(const float* row_lp, int n_rows, const int32_t* opt_off,
+                               int n_opts, const int32_t* q_off, int Q, const float* prior,
+                               float* scores, float* probs, int32_t* argmax, unsigned* err,
+                               void* stream);
+
 // One thread polls *flag until it equals `expect` or limit_ns (clamped to
 // 1 us .. kWaitLimitNs) passes; on timeout the device error word gets
 // kErrTimeout.

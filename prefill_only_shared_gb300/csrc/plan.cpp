@@ -702,6 +702,20 @@ extern "C" sp_status sp_check_labels(const int32_t* label_off, const int32_t* la
   return SP_OK;
 }
 
+extern "C" sp_status sp_check_options(const int32_t* opt_off, int32_t n_opts, int32_t n_rows,
+                                      const int32_t* q_off, int32_t n_questions) {
+  if (!opt_off || !q_off || n_opts < 2 || n_rows < 1 || n_questions < 1) return SP_ERR_ARG;
+  if (opt_off[0] != 0 || opt_off[n_opts] > n_rows || q_off[0] != 0 || q_off[n_questions] > n_opts)
+    return SP_ERR_ARG;
+  for (int32_t o = 0; o < n_opts; ++o)
+    if (opt_off[o + 1] <= opt_off[o]) return SP_ERR_ARG;
+  for (int32_t q = 0; q < n_questions; ++q) {
+    const int32_t k = q_off[q + 1] - q_off[q];
+    if (k < 2 || k > 64) return SP_ERR_ARG;
+  }
+  return SP_OK;
+}
+
 extern "C" const char* sp_status_str(sp_status s) {
   switch (s) {
     case SP_OK: return "ok";

@@ -197,6 +197,26 @@ class SharedPrefixClassifier:
         self.last_candidate_launches = sp.sp_last_launch_count()
         return dist, argmax, value, conf
 
+    def options(self, h_rows, W, opt_off, opt_tokens, q_off, prior=None, stream=None):
+        """Multi-token options: the readout with one label per row (each
+        option token at the position before it), then the option scores and
+        their (optionally prior-calibrated) softmax per question.  Returns
+        (row_logprobs, scores, probs, argmax)."""
+        stream = self._stream(stream)
+        n_rows = h_rows.shape[0]
+        row_off = self._buf("row_off", n_rows + 1, torch.int32)
+        if not getattr(self, "_row_off_n", None) == n_rows:
+            row_off.copy_(torch.arange(n_rows + 1, dtype=torch.int32, device=self.device))
+            self._row_off_n = n_rows
+        lp, _ = self.logprobs(h_rows, W, row_off, opt_tokens, n_rows, stream)
+        n_opts = opt_off.numel() - 1
+        scores = self._buf("opt_scores", n_opts, torch.float32)
+        probs = self._buf("opt_probs", n_opts, torch.float32)
+        argmax = self._buf("opt_argmax", q_off.numel() - 1, torch.int32)
+        sp.sp_option_softmax(lp, opt_off, q_off, scores, probs, argmax, prior, stream)
+        self.last_option_launches = self.last_logprob_launches + sp.sp_last_launch_count()
+        return lp, scores, probs, argmax
+
     def readout(self, h, W, label_off, label_ids, n_labels, stream=None, qtype=None):
         """LM-head label log-probabilities, then the label softmax; with
         ``qtype`` (device int32 [N]) the softmax is the fused decision and the

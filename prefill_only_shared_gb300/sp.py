@@ -86,6 +86,8 @@ SIGNATURES = {
     "sp_candidate_decide": (_I32, [_P, _P, _I32, _P, _P, _I32, _P, _P, _P, _P, _P]),
     "sp_wait_flag": (_I32, [_P, ctypes.c_uint32, ctypes.c_int64, _P]),
     "sp_check_labels": (_I32, [_I32P, _I32P, _I32, _I32]),
+    "sp_option_softmax": (_I32, [_P, _I32, _P, _I32, _P, _I32, _P, _P, _P, _P, _P]),
+    "sp_check_options": (_I32, [_I32P, _I32, _I32, _I32P, _I32]),
     "sp_check_device_error": (_I32, [_P]),
     "sp_status_str": (ctypes.c_char_p, [_I32]),
     "sp_last_launch_count": (_I32, []),
@@ -402,6 +404,29 @@ def sp_label_decide(logprobs, label_off, qtype, probs, argmax, value, confidence
         _dev(argmax, torch.int32, "argmax"), _dev(value, torch.float32, "value"),
         _dev(confidence, torch.float32, "confidence"), _stream(stream))
     _check(st, "sp_label_decide")
+
+
+def sp_option_softmax(row_logprobs, opt_off, q_off, scores, probs, argmax, prior=None,
+                      stream=None):
+    n_rows = row_logprobs.numel()
+    n_opts = opt_off.numel() - 1
+    Q = q_off.numel() - 1
+    if prior is not None and prior.numel() != n_opts:
+        raise ValueError("prior must have one entry per option")
+    st = lib().sp_option_softmax(
+        _dev(row_logprobs, torch.float32, "row_logprobs"), n_rows,
+        _dev(opt_off, torch.int32, "opt_off"), n_opts, _dev(q_off, torch.int32, "q_off"), Q,
+        _dev(prior, torch.float32, "prior") if prior is not None else None,
+        _dev(scores, torch.float32, "scores"), _dev(probs, torch.float32, "probs"),
+        _dev(argmax, torch.int32, "argmax"), _stream(stream))
+    _check(st, "sp_option_softmax")
+
+
+def sp_check_options(opt_off, n_rows: int, q_off):
+    oo = _np(opt_off, np.int32)
+    qo = _np(q_off, np.int32)
+    _check(lib().sp_check_options(oo.ctypes.data_as(_I32P), len(oo) - 1, int(n_rows),
+                                  qo.ctypes.data_as(_I32P), len(qo) - 1), "sp_check_options")
 
 
 def sp_candidate_decide(probs, label_off, cand_off, qtype, dist, argmax, value, confidence,

@@ -270,3 +270,56 @@ def small_case(trees, seed=0, n_q_heads=4, n_kv_heads=2, head_dim=64, hidden=128
         trees = [trees]
     shape = Shape(n_q_heads, n_kv_heads, head_dim, page_size, hidden, vocab)
     return make_workload("custom", seed=seed, trees=trees, shape=shape, label_spec=labels)
+
+
+@dataclass
+class OptionWorkload:
+    """Multi-token options: question q owns options q_off[q] .. q_off[q+1]-1,
+    option o owns rows opt_off[o] .. opt_off[o+1]-1, one row per option token:
+    the hidden state at the position before that token (h_rows, bf16) and the
+    token itself (tokens).  prior: a per-option log-probability for
+    calibration (fp32), drawn here as a stand-in for the readout of a
+    content-free input."""
+    hidden: int
+    vocab: int
+    h_rows: torch.Tensor
+    W: torch.Tensor | None
+    tokens: np.ndarray
+    opt_off: np.ndarray
+    q_off: np.ndarray
+    prior: np.ndarray
+
+    @property
+    def n_rows(self):
+        return int(self.opt_off[-1])
+
+    @property
+    def n_opts(self):
+        return len(self.opt_off) - 1
+
+    @property
+    def n_questions(self):
+        return len(self.q_off) - 1
+
+
+def make_options(seed: int = 0, n_questions: int = 16, opts=(2, 8), tokens=(1, 4),
+                 hidden: int = 2048, vocab: int = 151936, w_std: float = 0.02,
+                 with_W: bool = True) -> OptionWorkload:
+    """Seeded option workload.  Draw order (one torch.Generator): options per
+    question U{opts}, tokens per option U{tokens}, token ids uniform over the
+    vocabulary, h_rows ~ N(0, 1) bf16 [rows, hidden], prior ~ N(-ln vocab, 1)
+    fp32 per option, W ~ N(0, w_std) bf16 [vocab, hidden] (last, so
+    with_W=False, for a caller that has its LM head already, leaves every
+    other value unchanged)."""
+    g = torch.Generator().manual_seed(seed)
+    k = torch.randint(opts[0], opts[1] + 1, (n_questions,), generator=g)
+    q_off = np.concatenate([[0], np.cumsum(k.numpy())]).astype(np.int32)
+    n_opts = int(q_off[-1])
+    m = torch.randint(tokens[0], tokens[1] + 1, (n_opts,), generator=g)
+    opt_off = np.concatenate([[0], np.cumsum(m.numpy())]).astype(np.int32)
+    n_rows = int(opt_off[-1])
+    toks = torch.randint(0, vocab, (n_rows,), generator=g).numpy().astype(np.int32)
+    h_rows = torch.randn(n_rows, hidden, generator=g).bfloat16()
+    prior = (torch.randn(n_opts, generator=g) - float(np.log(vocab))).numpy().astype(np.float32)
+    W = (torch.randn(vocab, hidden, generator=g) * w_std).bfloat16() if with_W else None
+    return OptionWorkload(hidden, vocab, h_rows, W, toks, opt_off, q_off, prior)

@@ -156,3 +156,16 @@ def test_split_plan_covers_all_units(lib):
                              wl.tok_offsets, wl.tokens, 1 << 20, n_sms=152)
     st = plan.stats()
     assert st["attn_workspace_bytes"] > 0 and st["desc_bytes"] > 0
+
+
+def test_check_options(lib):
+    """Host validation of the option CSRs of sp_option_softmax."""
+    lib.sp_check_options([0, 1, 3, 4, 6], 6, [0, 2, 4])
+    for opt_off, n_rows, q_off in (([1, 2, 3], 3, [0, 2]),        # opt_off must start at 0
+                                   ([0, 1, 1, 2], 2, [0, 3]),     # an empty option
+                                   ([0, 1, 2], 1, [0, 2]),        # rows past n_rows
+                                   ([0, 1, 2, 3], 3, [0, 1, 3]),  # a question of 1 option
+                                   ([0, 1, 2], 2, [0, 3]),        # options past n_opts
+                                   ([0] + list(range(1, 67)), 66, [0, 66])):  # 66 options
+        with pytest.raises(lib.SpError):
+            lib.sp_check_options(opt_off, n_rows, q_off)
