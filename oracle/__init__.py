@@ -24,6 +24,9 @@ Everything is computed from the plain definition, in float64 with numpy:
                        question types).
 * ``cache``         -- the radix prefix cache across calls (LLM2Jev page,
                        section on reusing the radix cache).
+* ``batching``      -- the admission rule of continuous batching across
+                       requests (openjev-multimodal performance page, next
+                       steps).
 * ``options``       -- multi-token option scores (chain-rule sums of
                        readout log-probabilities) and label-prior calibration
                        (openjev-multimodal performance page, next steps).
