@@ -345,6 +345,46 @@ def run_libsp(args, ws, rank, local):
     opt_bytes = sh.vocab * sh.hidden * 2 + owl.n_rows * sh.hidden * 2 + owl.n_rows * 8
     opt_launches = clf.last_option_launches
 
+    # ---- continuous batching across requests ----------------------------------
+    # (a stream of independent yes/no-shaped requests, each with its own
+    # 2000-token prefix and 5 x 48 branches, queued before the timed region;
+    # batches of up to 16384 node tokens against one request per batch, the
+    # same stream and LM head)
+    from prefill_only_shared_gb300.pipeline import ContinuousBatcher
+    from prefill_only_shared_gb300.workloads import make_request_stream
+    n_stream = 32
+    stream_reqs = make_request_stream(n_stream, seed=1, shape=sh)
+    staged = [(r.tok_offsets, r.tokens, r.q.to(dev), r.k.to(dev), r.v.to(dev), r.h.to(dev),
+               r.label_off, r.label_ids) for r in stream_reqs]
+    rows_total = sum(int(r.q.shape[0]) for r in stream_reqs)
+    br_total = sum(len(r.tok_offsets) - 1 for r in stream_reqs)
+    lab_total = sum(int(r.label_off[-1]) for r in stream_reqs)
+    cb_ms, cb_batches = {}, {}
+    for mode, (budget, cap) in (("one_request_per_batch", (1, 1)), ("batched", (16384, 64))):
+        cb = ContinuousBatcher(clf, W, budget, cap, capacity_rows=rows_total,
+                               capacity_branches=br_total, capacity_labels=lab_total,
+                               schedule=args.schedule)
+        times = []
+        for rep in range(args.warmup + 3):
+            cb.reset()
+            for x in staged:
+                cb.submit(*x, stream=stream)
+            torch.cuda.synchronize()
+            c0 = torch.cuda.Event(enable_timing=True)
+            c1 = torch.cuda.Event(enable_timing=True)
+            c0.record(stream)
+            n_b = cb.run(stream)
+            c1.record(stream)
+            torch.cuda.synchronize()
+            if rep >= args.warmup:
+                times.append(c0.elapsed_time(c1))
+        sp.sp_check_device_error()
+        cb_ms[mode] = job_time(statistics.mean(times), ws, dev)
+        cb_batches[mode] = n_b
+        del cb
+    del staged
+    stream_branch_tokens = n_stream * 5 * 48
+
     # ---- end-to-end through the public call, host buffers --------------------
     pin = lambda x: x.pin_memory()
     hq, hk, hv, hh = pin(wl.q), pin(wl.k), pin(wl.v), pin(wl.h)
@@ -455,6 +495,23 @@ def run_libsp(args, ws, rank, local):
                          "note": "sp_label_logprobs over the option-token rows plus "
                                  "sp_option_softmax, timed together"},
             "gpu_launches_per_call": int(opt_launches),
+        },
+        "continuous_batching": {
+            "workload": f"{n_stream} independent yes/no-shaped requests (own 2000-token prefix, "
+                        f"5 x 48 branches, 2 labels each), queued; batches of up to 16384 node "
+                        f"tokens against one request per batch",
+            "batched": {"batches": cb_batches["batched"],
+                        "ms": round(cb_ms["batched"], 4),
+                        "requests_per_s": round(n_stream * ws / (cb_ms["batched"] / 1e3), 1),
+                        "decisions_per_s": round(br_total * ws / (cb_ms["batched"] / 1e3), 1),
+                        "branch_tokens_per_s": round(stream_branch_tokens * ws /
+                                                     (cb_ms["batched"] / 1e3), 1)},
+            "one_request_per_batch": {
+                "batches": cb_batches["one_request_per_batch"],
+                "ms": round(cb_ms["one_request_per_batch"], 4),
+                "requests_per_s": round(n_stream * ws / (cb_ms["one_request_per_batch"] / 1e3), 1),
+                "decisions_per_s": round(br_total * ws / (cb_ms["one_request_per_batch"] / 1e3), 1)},
+            "speedup": round(cb_ms["one_request_per_batch"] / cb_ms["batched"], 3),
         },
         "decisions_per_s": round(N * ws / (ms / 1e3), 1),
         "logical_tokens_per_s": round(stats["logical_tokens"] * ws / (ms / 1e3), 1),

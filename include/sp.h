@@ -171,6 +171,61 @@ sp_status sp_plan_build_cached(const sp_shape* shape, sp_cache* cache, int32_t n
  * use (their kernels write the pages).  Committing twice is a no-op. */
 sp_status sp_cache_commit(sp_cache* cache, sp_plan* plan);
 
+/* ---- continuous batching across requests ---------------------------------
+ *
+ * Source: openjev-multimodal "performance" page, section on next steps
+ * (continuous batching across requests, to raise throughput); the SGLang-JAX
+ * blog translation, section on reducing scheduling overhead (the host
+ * prepares the next batch while the device computes the current one) is
+ * prior art for the loop around it.  The pages give no admission rule; this
+ * library's reading:
+ *  - a request's size is its node tokens, the positions of its token trie
+ *    (every distinct prefix of its branches counted once: what its plan
+ *    computes cold);
+ *  - requests wait in a first-in first-out queue; a batch takes them from
+ *    the head, in submission order, while its node tokens stay within
+ *    max_batch_tokens and its request count within max_batch_requests; the
+ *    head request always goes in, so a request larger than the budget forms
+ *    a batch of its own;
+ *  - request i of a batch is request id i of the batch's plan (sp_plan_build
+ *    over the batch's branches), so its node rows, branches and labels
+ *    follow those of requests 0 .. i-1: a caller that stores each request's
+ *    inputs right after the previous one's reads a batch's inputs as one
+ *    contiguous slice.
+ * Requests never share K/V: a request's results do not depend on the batch it
+ * runs in.  Host-only; one thread uses a batcher at a time. */
+typedef struct sp_batcher sp_batcher;
+
+/* max_batch_tokens >= 1, max_batch_requests >= 1; shape as for sp_plan_build. */
+sp_status sp_batcher_create(const sp_shape* shape, int64_t max_batch_tokens,
+                            int32_t max_batch_requests, sp_batcher** out);
+void sp_batcher_free(sp_batcher* batcher);
+
+/* Enqueue one request: its n_branches token sequences (HOST CSR, copied).
+ * out_id (may be NULL) receives its id, 0, 1, 2, ... in submission order;
+ * out_node_tokens (may be NULL) its node tokens.  SP_ERR_ARG for an empty
+ * request or branch, SP_ERR_LIMIT for a branch over 32768 tokens or a
+ * request over 262144 tokens (checked here, before any batch forms). */
+sp_status sp_batcher_submit(sp_batcher* batcher, int32_t n_branches, const int64_t* tok_offsets,
+                            const int32_t* tokens, int64_t* out_id, int64_t* out_node_tokens);
+
+/* Requests and node tokens waiting in the queue. */
+sp_status sp_batcher_pending(const sp_batcher* batcher, int32_t* n_requests,
+                             int64_t* n_node_tokens);
+
+/* Form the next batch and build its plan (max_pages, n_sms as for
+ * sp_plan_build; free the plan with sp_plan_free).  On return *n_requests is
+ * the batch size (0 and *out_plan NULL when the queue is empty), and, as
+ * views valid until the next call: request_ids [n] (submission ids),
+ * branch_off [n+1] (request i owns the plan's branches branch_off[i] ..
+ * branch_off[i+1]-1) and row_off [n+1] (its node rows row_off[i] ..
+ * row_off[i+1]-1).  Any view pointer may be NULL.  When the plan cannot be
+ * built (SP_ERR_POOL_FULL for instance) the status is returned and the queue
+ * is left unchanged. */
+sp_status sp_batcher_next(sp_batcher* batcher, int32_t max_pages, int32_t n_sms,
+                          sp_plan** out_plan, int32_t* n_requests, const int64_t** request_ids,
+                          const int32_t** branch_off, const int64_t** row_off);
+
 sp_status sp_plan_get_stats(const sp_plan* plan, sp_plan_stats* out);
 
 /* Round lists: round r holds round_branches[round_offsets[r] .. round_offsets[r+1]),

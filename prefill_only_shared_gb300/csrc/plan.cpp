@@ -23,8 +23,8 @@
 
 namespace {
 
-constexpr int64_t kMaxBranchTokens = 32768;
-constexpr int64_t kMaxRequestTokens = 262144;
+using sp::kMaxBranchTokens;
+using sp::kMaxRequestTokens;
 constexpr int32_t kMinUnitsPerPart = 4;
 
 struct TNode {

@@ -29,6 +29,11 @@ struct sp_cache {
 };
 
 namespace sp {
+// Request limits (openjev-sglang article, section on the limits): tokens per
+// branch and logical tokens per request.
+constexpr int64_t kMaxBranchTokens = 32768;
+constexpr int64_t kMaxRequestTokens = 262144;
+
 // Longest cached prefix of seq[0, L): the (node, visible length) chain from
 // the root; returns the matched length.
 int64_t cache_match(const sp_cache& c, const int32_t* seq, int64_t L,

@@ -103,11 +103,13 @@ class SharedPrefixClassifier:
         self._ensure_pool(plan.stats()["pages_used"])
         return plan
 
-    def attention(self, plan, q, k, v, stream=None, schedule="rounds"):
+    def attention(self, plan, q, k, v, stream=None, schedule="rounds", out=None, lse=None):
         """schedule "rounds": one prefix and one branch call per staged round,
         in round order; "all": one prefix call and one branch call covering
         every round; "tree": one call for the whole trie.  Same results,
-        fewer launches."""
+        fewer launches.  out / lse: the caller's output tensors ([node
+        tokens, Hq, d] bf16, [node tokens, Hq] fp32), else the classifier's
+        own buffers."""
         stream = self._stream(stream)
         st = plan.stats()
         T = st["node_tokens"]
@@ -115,8 +117,10 @@ class SharedPrefixClassifier:
         desc = self._desc_view(st["desc_bytes"])
         sp.sp_plan_upload(plan, desc, stream)
         ws = self._buf("attn_ws", st["attn_workspace_bytes"], torch.uint8)
-        out = self._buf("out", T * Hq * d, torch.bfloat16).view(T, Hq, d)
-        lse = self._buf("lse", T * Hq, torch.float32).view(T, Hq)
+        if out is None:
+            out = self._buf("out", T * Hq * d, torch.bfloat16).view(T, Hq, d)
+        if lse is None:
+            lse = self._buf("lse", T * Hq, torch.float32).view(T, Hq)
         launches = 0
         if schedule == "tree":
             sp.sp_tree_attn(plan, desc, sp.SP_ALL_ROUNDS, q, k, v, self.kv_pool, out, lse, ws,
@@ -246,3 +250,178 @@ class SharedPrefixClassifier:
     def last_launches(self) -> int:
         return (getattr(self, "last_attention_launches", 0) + getattr(self, "last_logprob_launches", 0)
                 + getattr(self, "last_softmax_launches", 0))
+
+
+@dataclass
+class _Req:
+    row0: int
+    n_rows: int
+    br0: int
+    n_br: int
+    lab0: int
+    label_off: np.ndarray  # the request's own label CSR offsets (from 0)
+
+
+class ContinuousBatcher:
+    """Continuous batching of independent requests over one classifier.
+
+    Requests are queued first-in first-out by a native batcher (include/sp.h,
+    sp_batcher_*): each batch takes requests from the head of the queue while
+    its node tokens stay within ``max_batch_tokens`` and its size within
+    ``max_batch_requests``, and gets one plan, one attention call and one
+    readout for all its requests.  Requests never share K/V, so a request's
+    results do not depend on its batch; what batching saves is the LM head,
+    streamed once per batch instead of once per request, and attention grids
+    that fill the GPU.
+
+    ``submit`` stores a request's inputs right after the previous request's in
+    device arenas sized at construction (its q / k / v rows in the node-token
+    order of its own plan, its final hidden states, its label ids), so a batch
+    of consecutive requests reads one contiguous slice of each: nothing is
+    gathered.  ``run`` forms and enqueues the batches on one stream; planning a
+    batch on the host overlaps the GPU's work on the previous one.  Results
+    stay in the arenas until ``reset``.
+    """
+
+    def __init__(self, clf: SharedPrefixClassifier, W, max_batch_tokens: int,
+                 max_batch_requests: int = 64, capacity_rows: int = 1 << 15,
+                 capacity_branches: int = 4096, capacity_labels: int = 1 << 16,
+                 schedule: str = "tree"):
+        if clf.cache is not None:
+            raise ValueError("continuous batching plans without a prefix cache: use a classifier "
+                             "built without prefix_cache_pages")
+        s = clf.shape
+        dev = clf.device
+        self.clf, self.W, self.schedule = clf, W, schedule
+        self._live_plans = []
+        self.batcher = sp.Batcher(s, max_batch_tokens, max_batch_requests)
+        self.q = torch.empty(capacity_rows, s.n_q_heads, s.head_dim, dtype=torch.bfloat16, device=dev)
+        self.k = torch.empty(capacity_rows, s.n_kv_heads, s.head_dim, dtype=torch.bfloat16, device=dev)
+        self.v = torch.empty_like(self.k)
+        self.out = torch.empty_like(self.q)
+        self.lse = torch.empty(capacity_rows, s.n_q_heads, dtype=torch.float32, device=dev)
+        self.h = torch.empty(capacity_branches, s.hidden, dtype=torch.bfloat16, device=dev)
+        self.label_ids = torch.empty(capacity_labels, dtype=torch.int32, device=dev)
+        self.logprobs = torch.empty(capacity_labels, dtype=torch.float32, device=dev)
+        self.probs = torch.empty(capacity_labels, dtype=torch.float32, device=dev)
+        self.lse_vocab = torch.empty(capacity_branches, dtype=torch.float32, device=dev)
+        self.argmax = torch.empty(capacity_branches, dtype=torch.int32, device=dev)
+        # batch label offsets: a small ring of pinned host slots and device
+        # copies, a slot reused only once its last copy has completed
+        self._ring = [(torch.empty(capacity_branches + 1, dtype=torch.int32).pin_memory(),
+                       torch.empty(capacity_branches + 1, dtype=torch.int32, device=dev),
+                       torch.cuda.Event()) for _ in range(4)]
+        self._ring_used = [False] * 4
+        self._n_batches = 0
+        self.reset()
+
+    def reset(self):
+        """Forget every request and result (call with nothing in flight)."""
+        self._reqs = {}
+        self._rows = self._brs = self._labs = 0
+        self.batch_sizes = []
+
+    def submit(self, tok_offsets, tokens, q, k, v, h, label_off, label_ids, stream=None):
+        """Queue one request: its branches as a CSR of token ids (host), its
+        q / k / v rows in the node-token order of its own plan, its final
+        hidden states [branches, H] and its label CSR (host offsets, ids).
+        The tensors may live on the host (pinned for an asynchronous copy) or
+        on the device.  Returns the request id."""
+        rid, nt = self.batcher.submit(tok_offsets, tokens)
+        off = np.asarray(label_off, dtype=np.int64)
+        nb, nl = len(off) - 1, int(off[-1])
+        if q.shape[0] != nt or k.shape[0] != nt or v.shape[0] != nt or h.shape[0] != nb:
+            raise ValueError("q/k/v need one row per node token, h one row per branch")
+        if (self._rows + nt > self.q.shape[0] or self._brs + nb > self.h.shape[0]
+                or self._labs + nl > self.label_ids.shape[0]):
+            raise ValueError("ContinuousBatcher arenas are full: reset() or raise the capacities")
+        st = self._torch_stream(stream)
+        with torch.cuda.stream(st):
+            r0, b0, l0 = self._rows, self._brs, self._labs
+            self.q[r0:r0 + nt].copy_(q, non_blocking=True)
+            self.k[r0:r0 + nt].copy_(k, non_blocking=True)
+            self.v[r0:r0 + nt].copy_(v, non_blocking=True)
+            self.h[b0:b0 + nb].copy_(h, non_blocking=True)
+            self.label_ids[l0:l0 + nl].copy_(torch.as_tensor(np.asarray(label_ids, np.int32)),
+                                             non_blocking=True)
+        self._reqs[rid] = _Req(r0, nt, b0, nb, l0, off)
+        self._rows, self._brs, self._labs = r0 + nt, b0 + nb, l0 + nl
+        return rid
+
+    def _torch_stream(self, stream):
+        if stream is None:
+            return torch.cuda.current_stream(self.clf.device)
+        if isinstance(stream, torch.cuda.Stream):
+            return stream
+        return torch.cuda.ExternalStream(int(stream), device=self.clf.device)
+
+    def run(self, stream=None) -> int:
+        """Form and enqueue every batch of the queue on `stream`; returns the
+        number of batches.  Asynchronous: synchronise before reading results."""
+        st = self._torch_stream(stream)
+        raw = st.cuda_stream
+        clf = self.clf
+        V = self.W.shape[0]
+        n = 0
+        while True:
+            # planning here overlaps the GPU's work on the previous batch
+            nxt = self.batcher.next(clf.max_pages, clf.n_sms)
+            if nxt is None:
+                break
+            plan, ids, boff, roff = nxt
+            first = self._reqs[int(ids[0])]
+            for i, rid in enumerate(ids):  # consecutive requests, consecutive rows
+                r = self._reqs[int(rid)]
+                if r.row0 != first.row0 + roff[i] or r.br0 != first.br0 + boff[i]:
+                    raise RuntimeError("batch requests are not stored consecutively")
+            if not clf.fixed_pool:
+                clf._ensure_pool(plan.stats()["pages_used"])
+            rows = slice(first.row0, first.row0 + int(roff[-1]))
+            nb = int(boff[-1])
+            brs = slice(first.br0, first.br0 + nb)
+            clf.attention(plan, self.q[rows], self.k[rows], self.v[rows], raw, self.schedule,
+                          self.out[rows], self.lse[rows])
+            # the batch's label CSR, offsets from 0
+            offs = [0]
+            for rid in ids:
+                o = self._reqs[int(rid)].label_off
+                offs.extend((offs[-1] + o[1:]).tolist())
+            nl = offs[-1]
+            slot = self._n_batches % len(self._ring)
+            host, dev_off, ev = self._ring[slot]
+            if self._ring_used[slot]:
+                ev.synchronize()  # the slot's previous copy has been read
+            host[:nb + 1].numpy()[:] = np.asarray(offs, dtype=np.int32)
+            with torch.cuda.stream(st):
+                dev_off[:nb + 1].copy_(host[:nb + 1], non_blocking=True)
+                ev.record(st)
+            self._ring_used[slot] = True
+            labs = slice(first.lab0, first.lab0 + nl)
+            ws = clf._buf("lm_ws", sp.sp_label_workspace_bytes(nb, V, clf.n_sms), torch.uint8)
+            sp.sp_label_logprobs(self.h[brs], self.W, dev_off[:nb + 1], self.label_ids[labs], nl,
+                                 self.logprobs[labs], self.lse_vocab[brs], ws, raw)
+            sp.sp_label_softmax(self.logprobs[labs], dev_off[:nb + 1], self.probs[labs],
+                                self.argmax[brs], raw)
+            self.batch_sizes.append(len(ids))
+            self._n_batches += 1
+            n += 1
+            # the plan's descriptor is copied on the stream from the plan's host
+            # memory: keep the plan until the batch's work has passed that copy
+            done = torch.cuda.Event()
+            done.record(st)
+            self._live_plans = [(p, e) for p, e in self._live_plans if not e.query()]
+            self._live_plans.append((plan, done))
+        return n
+
+    def result(self, rid: int) -> dict:
+        """A request's outputs as views of the device arenas: attention out /
+        lse (its node rows, in its own plan's node-token order), label
+        log-probabilities, vocabulary lse, probabilities and argmax."""
+        r = self._reqs[rid]
+        nl = int(r.label_off[-1])
+        rows = slice(r.row0, r.row0 + r.n_rows)
+        labs = slice(r.lab0, r.lab0 + nl)
+        brs = slice(r.br0, r.br0 + r.n_br)
+        return {"out": self.out[rows], "lse": self.lse[rows], "logprobs": self.logprobs[labs],
+                "lse_vocab": self.lse_vocab[brs], "probs": self.probs[labs],
+                "argmax": self.argmax[brs]}

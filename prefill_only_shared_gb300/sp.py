@@ -65,6 +65,12 @@ SIGNATURES = {
     "sp_plan_build_cached": (_I32, [ctypes.POINTER(sp_shape), _P, _I32, _I32P, _I64P, _I32P, _I32,
                                     ctypes.POINTER(_P)]),
     "sp_cache_commit": (_I32, [_P, _P]),
+    "sp_batcher_create": (_I32, [ctypes.POINTER(sp_shape), ctypes.c_int64, _I32, ctypes.POINTER(_P)]),
+    "sp_batcher_free": (None, [_P]),
+    "sp_batcher_submit": (_I32, [_P, _I32, _I64P, _I32P, _I64P, _I64P]),
+    "sp_batcher_pending": (_I32, [_P, _I32P, _I64P]),
+    "sp_batcher_next": (_I32, [_P, _I32, _I32, ctypes.POINTER(_P), _I32P, ctypes.POINTER(_I64P),
+                               ctypes.POINTER(_I32P), ctypes.POINTER(_I64P)]),
     "sp_plan_get_stats": (_I32, [_P, ctypes.POINTER(sp_plan_stats)]),
     "sp_plan_rounds": (_I32, [_P, _I32P, ctypes.POINTER(_I32P), ctypes.POINTER(_I32P)]),
     "sp_plan_segments": (_I32, [_P, _I32P] + [ctypes.POINTER(_I32P)] * 2 + [ctypes.POINTER(_I64P)]
@@ -272,6 +278,62 @@ class Cache:
         try:
             if self._ptr:
                 lib().sp_cache_free(self._ptr)
+                self._ptr = None
+        except Exception:
+            pass
+
+
+class Batcher:
+    """Owns an sp_batcher*: the first-in first-out request queue of continuous
+    batching and its admission rule (max_batch_tokens node tokens and
+    max_batch_requests requests per batch).  Host-only; one thread at a time."""
+
+    def __init__(self, shape: sp_shape, max_batch_tokens: int, max_batch_requests: int):
+        self._ptr = None
+        self.shape = shape
+        out = ctypes.c_void_p()
+        _check(lib().sp_batcher_create(ctypes.byref(shape), int(max_batch_tokens),
+                                       int(max_batch_requests), ctypes.byref(out)),
+               "sp_batcher_create")
+        self._ptr = out
+
+    def submit(self, tok_offsets, tokens):
+        """Enqueue a request (its branches as a CSR of token ids); returns
+        (request id, node tokens)."""
+        off = _np(tok_offsets, np.int64)
+        tok = _np(tokens, np.int32)
+        rid, nt = ctypes.c_int64(), ctypes.c_int64()
+        _check(lib().sp_batcher_submit(self._ptr, len(off) - 1, off.ctypes.data_as(_I64P),
+                                       tok.ctypes.data_as(_I32P), ctypes.byref(rid),
+                                       ctypes.byref(nt)), "sp_batcher_submit")
+        return int(rid.value), int(nt.value)
+
+    def pending(self):
+        n, t = ctypes.c_int32(), ctypes.c_int64()
+        _check(lib().sp_batcher_pending(self._ptr, ctypes.byref(n), ctypes.byref(t)),
+               "sp_batcher_pending")
+        return int(n.value), int(t.value)
+
+    def next(self, max_pages: int = (1 << 31) - 1, n_sms: int = 0):
+        """The next batch: (plan, request ids, branch offsets, row offsets) as
+        a Plan and numpy copies, or None when the queue is empty."""
+        plan = ctypes.c_void_p()
+        n = ctypes.c_int32()
+        ids, boff, roff = _I64P(), _I32P(), _I64P()
+        _check(lib().sp_batcher_next(self._ptr, int(max_pages), int(n_sms), ctypes.byref(plan),
+                                     ctypes.byref(n), ctypes.byref(ids), ctypes.byref(boff),
+                                     ctypes.byref(roff)), "sp_batcher_next")
+        k = int(n.value)
+        if k == 0:
+            return None
+        return (Plan(plan, self.shape), np.ctypeslib.as_array(ids, (k,)).copy(),
+                np.ctypeslib.as_array(boff, (k + 1,)).copy(),
+                np.ctypeslib.as_array(roff, (k + 1,)).copy())
+
+    def __del__(self):
+        try:
+            if self._ptr:
+                lib().sp_batcher_free(self._ptr)
                 self._ptr = None
         except Exception:
             pass

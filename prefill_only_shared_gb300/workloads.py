@@ -323,3 +323,52 @@ def make_options(seed: int = 0, n_questions: int = 16, opts=(2, 8), tokens=(1, 4
     prior = (torch.randn(n_opts, generator=g) - float(np.log(vocab))).numpy().astype(np.float32)
     W = (torch.randn(vocab, hidden, generator=g) * w_std).bfloat16() if with_W else None
     return OptionWorkload(hidden, vocab, h_rows, W, toks, opt_off, q_off, prior)
+
+
+@dataclass
+class Request:
+    """One request of a stream: branch token CSR, q / k / v in the node-token
+    order of its own plan, final hidden states and label CSR (CPU)."""
+    tok_offsets: np.ndarray
+    tokens: np.ndarray
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    h: torch.Tensor
+    label_off: np.ndarray
+    label_ids: np.ndarray
+
+
+def make_request_stream(n_requests: int, seed: int = 0, prefix: int = 2000, n_branches: int = 5,
+                        suffix: int = 48, shape: Shape | None = None,
+                        n_labels: int = 2) -> list:
+    """Independent requests shaped like the yes/no configuration (a shared
+    prefix and n_branches suffixes), for continuous batching; the LM head is
+    the caller's.  Draw order per request (one torch.Generator): prefix
+    tokens, each suffix's tokens (its first token redrawn until distinct from
+    the earlier suffixes' first tokens), q, k, v ~ N(0, 1) bf16 in node-token
+    order (prefix rows, then each suffix's rows), h ~ N(0, 1) bf16, label ids
+    (distinct per branch)."""
+    sh = shape or Shape(32, 4, 128, 16, 2048, 151936)
+    g = torch.Generator().manual_seed(seed)
+    out = []
+    for _ in range(n_requests):
+        pre = torch.randint(0, sh.vocab, (prefix,), generator=g)
+        sufs, firsts = [], set()
+        for _ in range(n_branches):
+            s = torch.randint(0, sh.vocab, (suffix,), generator=g)
+            while int(s[0]) in firsts:
+                s[0] = torch.randint(0, sh.vocab, (1,), generator=g)
+            firsts.add(int(s[0]))
+            sufs.append(s)
+        seqs = [torch.cat([pre, s]).numpy().astype(np.int32) for s in sufs]
+        off = np.concatenate([[0], np.cumsum([len(s) for s in seqs])]).astype(np.int64)
+        T = prefix + n_branches * suffix
+        q = torch.randn(T, sh.n_q_heads, sh.head_dim, generator=g).bfloat16()
+        k = torch.randn(T, sh.n_kv_heads, sh.head_dim, generator=g).bfloat16()
+        v = torch.randn(T, sh.n_kv_heads, sh.head_dim, generator=g).bfloat16()
+        h = torch.randn(n_branches, sh.hidden, generator=g).bfloat16()
+        ids = np.concatenate([_draw_distinct(g, sh.vocab, n_labels) for _ in range(n_branches)])
+        loff = np.arange(0, n_labels * (n_branches + 1), n_labels, dtype=np.int32)
+        out.append(Request(off, np.concatenate(seqs), q, k, v, h, loff, ids.astype(np.int32)))
+    return out
