@@ -210,7 +210,7 @@ class SharedPrefixClassifier:
         n_rows = h_rows.shape[0]
         row_off = self._buf("row_off", n_rows + 1, torch.int32)
         if not getattr(self, "_row_off_n", None) == n_rows:
-            row_off.copy_(torch.arange(n_rows + 1, dtype=torch.int32, device=self.device))
+            row_off.copy_(torch.arange(n_rows + 1, dtype=torch.int32))  # host index, copied
             self._row_off_n = n_rows
         lp, _ = self.logprobs(h_rows, W, row_off, opt_tokens, n_rows, stream)
         n_opts = opt_off.numel() - 1
