@@ -369,15 +369,15 @@ sp_status sp_label_logprobs(const void* h, const void* W, int32_t N, int32_t H, 
  * No counterpart in the pages: this is a property of this library only.
  *
  * The readout's scratch (one partial max / sum-of-exp pair per CTA and
- * branch, and a grid-barrier counter that each call zeroes before its
- * launch) lives in a static device array of SP_NOALLOC_SCRATCH_BYTES inside
+ * branch, and two counters, the grid barrier's and the one that hands out
+ * the last vocabulary tiles, which each call zeroes before its launch) lives in a static device array of SP_NOALLOC_SCRATCH_BYTES inside
  * the library; every GPU that loads the library holds it until the process
  * exits.  Limit: N <= SP_NOALLOC_MAX_BRANCHES; a larger N returns
  * SP_ERR_WORKSPACE and launches nothing.  The first call on each device looks
  * up the array's device address (a runtime query, no allocation); make that
  * first call before any stream capture.  All calls share the one array and it
- * keeps the last call's contents; the only part that must start at zero, the
- * barrier counter, is cleared by each call on its stream before its launch,
+ * keeps the last call's contents; the only parts that must start at zero,
+ * the two counters, are cleared by each call on its stream before its launch,
  * and every other entry a call reads is written by that call.  Calls that can
  * overlap on the GPU (different streams without ordering, or several threads)
  * race on the array and must be serialised by the caller.  Arguments, results

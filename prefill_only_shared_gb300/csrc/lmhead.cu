@@ -14,6 +14,11 @@
 //               thread), per-column max / sum-of-exp over the 128 rows, merged
 //               into a running (max, sum) per branch; label logits picked out
 //               of TMEM when a label id falls in the tile.
+// Work: vocab tiles x branch chunks ("units").  Each CTA first takes a fixed
+// run of units, all CTAs together all but about two per CTA; the rest are
+// taken one at a time from a global counter, so CTAs on SMs that stream
+// faster take more of them.  The producer publishes each unit's index in a
+// small shared-memory ring for the issuer and the epilogue.
 // After a grid barrier (cooperative launch, one CTA per SM), every warp of
 // the grid merges the per-CTA (max, sum) pairs of some branches into lse and
 // turns their label logits into log-probabilities.
@@ -48,8 +53,20 @@ struct LmArgs {
   float* lse;         // [N]
   float2* partials;   // [gridDim.x][N]
   unsigned* grid_arrivals;  // zero at launch
+  unsigned* unit_counter;   // zero at launch: units taken from the shared tail
+  int n_static;             // units of each CTA's fixed run
   unsigned* err;
 };
+
+constexpr int kUnitRing = 4;  // unit indices published ahead of the consumers
+
+// A load with acquire semantics at GPU scope (a polling read of a flag that
+// other CTAs update with atomics).
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
     lmhead_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmH,
@@ -64,9 +81,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_full = empty + a.stages;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* unit_full = drain + 1;             // [kUnitRing]: a unit index is published
+  uint64_t* unit_empty = unit_full + kUnitRing;  // [kUnitRing]: read by the issuer and 4 epilogue warps
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(unit_empty + kUnitRing);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float2* state = reinterpret_cast<float2*>(tmem_slot + 4);  // [4][N]
+  int* unit_ring = reinterpret_cast<int*>(tmem_slot + 2);  // [kUnitRing], -1 ends the sequence
+  int* dyn_count = unit_ring + kUnitRing;                  // labels of the shared tail's rows
+  float2* state = reinterpret_cast<float2*>(tmem_slot + 8);  // [4][N]
   // labels whose id falls in this CTA's vocab rows (indices into label_ids),
   // the branch of every label j < lab_cap, and the list length
   int32_t* lab_list = reinterpret_cast<int32_t*>(state + 4 * a.N);     // [lab_cap]
@@ -74,8 +95,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* lab_count = reinterpret_cast<int*>(lab_br + ((a.lab_cap + 1) & ~1));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int u_begin = (int)((int64_t)a.n_units * blockIdx.x / gridDim.x);
-  const int u_end = (int)((int64_t)a.n_units * (blockIdx.x + 1) / gridDim.x);
+  // this CTA's fixed run of units, then the shared tail [tail_lo, n_units)
+  const int u_begin = blockIdx.x * a.n_static;
+  const int u_end = u_begin + a.n_static;
+  const int tail_lo = (int)gridDim.x * a.n_static;
   const int nk = (a.H + kKT - 1) / kKT;
 
   if (threadIdx.x == 0) {
@@ -88,8 +111,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&acc_empty[b], 128);
     }
     mbar_init(drain, 1);
+    for (int r = 0; r < kUnitRing; ++r) {
+      mbar_init(&unit_full[r], 1);
+      mbar_init(&unit_empty[r], 5);
+    }
     *abort_flag = 0;
     *lab_count = 0;
+    *dyn_count = 0;
     fence_barrier_init();
     prefetch_tensormap(&tmW);
     prefetch_tensormap(&tmH);
@@ -121,7 +149,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     int issued_phase[kMaxStages];
     for (int i = 0; i < kMaxStages; ++i) issued_phase[i] = -1;
     bool ok = true;
-    for (int u = u_begin; u < u_end && ok; ++u) {
+    for (int i = 0; ok; ++i) {
+      // the unit: the fixed run first, then the shared tail
+      int u = u_begin + i;
+      if (i >= a.n_static) {
+        u = tail_lo + (int)atomicAdd(a.unit_counter, 1u);
+        if (u >= a.n_units) u = -1;
+      }
+      const int r = i % kUnitRing;
+      const uint32_t ruse = (uint32_t)(i / kUnitRing);
+      if (ruse > 0 && !mbar_wait(&unit_empty[r], (ruse - 1) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      unit_ring[r] = u;
+      mbar_arrive(&unit_full[r]);  // releases the write above
+      if (u < 0) break;
       const int t = u / a.n_ch, c = u % a.n_ch;
       for (int k = 0; k < nk; ++k) {
         if (!mbar_wait(&empty[s], ph ^ 1, abort_flag)) {
@@ -152,7 +195,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
-    for (int u = u_begin, i = 0; u < u_end && ok; ++u, ++i) {
+    for (int i = 0; ok; ++i) {
+      const int r = i % kUnitRing;
+      if (!mbar_wait(&unit_full[r], (uint32_t)(i / kUnitRing) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      const int u = unit_ring[r];
+      mbar_arrive(&unit_empty[r]);
+      if (u < 0) break;
       const int b = i & 1;
       const uint32_t use = (uint32_t)(i >> 1);
       if (!mbar_wait(&acc_empty[b], (use & 1) ^ 1, abort_flag)) {
@@ -192,23 +243,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- epilogue ----------------
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     float2* st = state + q * a.N;
-    // The labels whose id lies in this CTA's vocab rows, once (the stream is
-    // already filling the pipeline); each tile then checks only those.
+    // The labels whose id lies in this CTA's fixed run of vocab rows, and
+    // those in the shared tail's rows, once (the stream is already filling
+    // the pipeline): the first list from the front of lab_list, the second
+    // from its back; each tile then checks only its list.
     {
       const int v_lo = (u_begin / a.n_ch) * kVT;
       const int v_hi = u_end > u_begin ? ((u_end - 1) / a.n_ch + 1) * kVT : v_lo;
+      const int t_lo = (tail_lo / a.n_ch) * kVT;
       for (int j = threadIdx.x - 64; j < a.n_labels; j += 128) {
         const int id = a.label_ids[j];
         if (id >= v_lo && id < v_hi) {
           const int k = atomicAdd(lab_count, 1);
           if (k < a.lab_cap) lab_list[k] = j;
         }
+        if (id >= t_lo && tail_lo < a.n_units) {
+          const int k = atomicAdd(dyn_count, 1);
+          if (k < a.lab_cap) lab_list[a.lab_cap - 1 - k] = j;
+        }
       }
       asm volatile("bar.sync 1, 128;" ::: "memory");
     }
-    const int n_local = *lab_count;
-    const bool use_list = n_local <= a.lab_cap;
-    for (int u = u_begin, i = 0; u < u_end; ++u, ++i) {
+    const int n_fixed = *lab_count, n_tail = *dyn_count;
+    const bool use_list = n_fixed + n_tail <= a.lab_cap;
+    for (int i = 0;; ++i) {
+      const int r = i % kUnitRing;
+      if (!__all_sync(0xffffffffu, mbar_wait(&unit_full[r], (uint32_t)(i / kUnitRing) & 1, abort_flag))) {
+        if (!*abort_flag) raise_error(a.err, kErrTimeout);
+        *abort_flag = 1;
+        break;
+      }
+      const int u = unit_ring[r];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&unit_empty[r]);  // after every lane's read
+      if (u < 0) break;
+      const bool in_tail = u >= tail_lo;
+      const int n_local = in_tail ? n_tail : n_fixed;
       const int b = i & 1;
       const uint32_t use = (uint32_t)(i >> 1);
       if (!mbar_wait(&acc_full[b], use & 1, abort_flag)) {
@@ -252,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int j_hi = use_list ? n_local : a.label_off[n_hi];
       for (int jb = j_lo; jb < j_hi; jb += 32) {
         const int e = jb + lane;
-        const int j = e < j_hi ? (use_list ? lab_list[e] : e) : -1;
+        const int j = e < j_hi ? (use_list ? lab_list[in_tail ? a.lab_cap - 1 - e : e] : e) : -1;
         const int id = j >= 0 ? a.label_ids[j] : -1;
         bool match = id >= v_base && id < v_base + 32 && id < a.V;
         int br = -1;
@@ -310,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     atomicAdd(a.grid_arrivals, 1u);
     const unsigned long long t0 = globaltimer();
     int ok = 1;
-    while (atomicAdd(a.grid_arrivals, 0u) < gridDim.x) {
+    while (ld_acquire_gpu(a.grid_arrivals) < gridDim.x) {
       if (globaltimer() - t0 > kWaitLimitNs) {
         raise_error(a.err, kErrTimeout);
         ok = 0;
@@ -367,7 +437,8 @@ Geometry geometry(int N, int V, int n_sms, int n_labels = 0) {
   g.n_units = n_vt * g.n_ch;
   g.grid = n_sms < g.n_units ? n_sms : g.n_units;
   const size_t stage = (size_t)kWBytes + (size_t)g.nc * kKT * 2;
-  const size_t base = 1024 /*align slack*/ + (2 * kMaxStages + 5) * 8 + 16 + (size_t)4 * N * 8;
+  const size_t base = 1024 /*align slack*/ + (2 * kMaxStages + 5 + 2 * kUnitRing) * 8 + 32 +
+                      (size_t)4 * N * 8;
   // the label cache takes only what is left after min(4, stages that fit
   // without it) pipeline stages
   const int st_free = base < kSmemCap ? (int)((kSmemCap - base) / stage) : 0;
@@ -400,7 +471,8 @@ bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t oute
 
 }  // namespace
 
-// Workspace: per-CTA partials [grid][N] float2, then the grid-barrier counter.
+// Workspace: per-CTA partials [grid][N] float2, then the grid-barrier counter
+// and the shared-tail unit counter (both zeroed by each call).
 size_t lmhead_workspace_bytes(int N, int V, int n_sms) {
   Geometry g = geometry(N, V, n_sms > 0 ? n_sms : 152);
   return ((size_t)g.grid * N * sizeof(float2) + 16 + 255) & ~size_t(255);
@@ -429,12 +501,15 @@ cudaError_t lmhead_run(const LmheadLaunch& L) {
   a.logits_out = L.logprobs;
   a.partials = static_cast<float2*>(L.workspace);
   a.grid_arrivals = reinterpret_cast<unsigned*>(a.partials + (size_t)g.grid * L.N);
+  a.unit_counter = a.grid_arrivals + 1;
+  // a fixed run per CTA; the last units (about two per CTA) are shared
+  a.n_static = g.n_units / g.grid > 1 ? g.n_units / g.grid - 1 : 0;
   a.lse = L.lse;
   a.err = L.err;
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(lmhead_kernel), (int)g.smem);
   if (e != cudaSuccess) return e;
   cudaStream_t st = static_cast<cudaStream_t>(L.stream);
-  e = cudaMemsetAsync(a.grid_arrivals, 0, sizeof(unsigned), st);
+  e = cudaMemsetAsync(a.grid_arrivals, 0, 2 * sizeof(unsigned), st);
   if (e != cudaSuccess) return e;
   void* args[] = {&tmW, &tmH, &a};
   e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(lmhead_kernel), dim3(g.grid),
@@ -445,9 +520,9 @@ cudaError_t lmhead_run(const LmheadLaunch& L) {
 }
 
 // ---------------------------------------------------------------------------
-// No-allocation readout: the per-CTA partials and the grid-barrier counter
-// live in this file-scope device array (2 MiB + 256 bytes: up to 256 CTAs x
-// 1024 branches x one float2, then the counter), which every GPU
+// No-allocation readout: the per-CTA partials and the two counters live in
+// this file-scope device array (2 MiB + 256 bytes: up to 256 CTAs x 1024
+// branches x one float2, then the counters), which every GPU
 // that loads the library holds until exit.  Host code cannot use the array's
 // name as a device address, so its address is looked up once per device (with
 // that device current) and passed to the kernel like any workspace.  Calls
@@ -455,7 +530,7 @@ cudaError_t lmhead_run(const LmheadLaunch& L) {
 // clearing, and overlapping calls would race.
 namespace {
 constexpr size_t kNoallocScratchBytes =
-    (size_t)kNoallocMaxCtas * kNoallocMaxBranches * sizeof(float2) + 256;  // + barrier counter
+    (size_t)kNoallocMaxCtas * kNoallocMaxBranches * sizeof(float2) + 256;  // + the counters
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
 cudaError_t noalloc_scratch_address(void** out) {
