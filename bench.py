@@ -392,19 +392,15 @@ def run_libsp(args, ws, rank, local):
     hids = pin(torch.from_numpy(wl.label_ids))
     out_probs = torch.empty(n_labels, dtype=torch.float32).pin_memory()
     out_am = torch.empty(N, dtype=torch.int32).pin_memory()
-    dq, dk, dv, dh = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(h)
-    doff, dids = torch.empty_like(off), torch.empty_like(ids)
     h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hh, hoff, hids))
     h2d += wl.tokens.nbytes + wl.tok_offsets.nbytes + wl.req_of_branch.nbytes  # read by the planner
     d2h = out_probs.numel() * 4 + out_am.numel() * 4
 
     def e2e_step():
-        for d_, s_ in ((dq, hq), (dk, hk), (dv, hv), (dh, hh), (doff, hoff), (dids, hids)):
-            d_.copy_(s_, non_blocking=True)
-        res = clf.run(wl.req_of_branch, wl.tok_offsets, wl.tokens, dq, dk, dv, dh, W, doff, dids,
-                      stream, args.schedule)
-        out_probs.copy_(res.probs, non_blocking=True)
-        out_am.copy_(res.argmax, non_blocking=True)
+        # inputs copied in from pinned host memory every step (on a side stream,
+        # overlapping the previous step's kernels), results copied out
+        clf.run_from_host(wl.req_of_branch, wl.tok_offsets, wl.tokens, hq, hk, hv, hh, W, hoff,
+                          hids, out_probs, out_am, stream, args.schedule)
 
     e2e_ms = float("nan")
     if args.e2e_steps > 0:
@@ -416,6 +412,7 @@ def run_libsp(args, ws, rank, local):
         if ws > 1:
             torch.distributed.barrier()
         e0.record(stream)
+        clf._copy_stream.wait_event(e0)  # the timed steps' copies start after e0
         for _ in range(args.e2e_steps):
             e2e_step()
         e1.record(stream)

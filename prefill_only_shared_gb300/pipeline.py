@@ -246,6 +246,62 @@ class SharedPrefixClassifier:
             h, W, label_off, label_ids, n_labels, stream, qtype)
         return PassOutputs(out, lse, logprobs, lse_v, probs, argmax, plan, value, conf)
 
+    def run_from_host(self, req_of_branch, tok_offsets, tokens, q, k, v, h, W, label_off,
+                      label_ids, probs_out, argmax_out, stream=None, schedule="rounds",
+                      qtype=None) -> PassOutputs:
+        """``run`` with the inputs in host memory: q, k, v, h, label_off and
+        label_ids (pinned, for asynchronous copies) are copied in on a side
+        stream into the next of two device input sets, so this call's copies
+        overlap the previous call's kernels; the pass runs on `stream` once
+        its copies are done, and its probabilities and argmax are copied out
+        into probs_out / argmax_out (pinned host tensors).  Asynchronous:
+        synchronise `stream` before reading the outputs.  W stays on the
+        device (model state)."""
+        st = self._torch_stream(stream)
+        if getattr(self, "_copy_stream", None) is None:
+            self._copy_stream = torch.cuda.Stream(self.device)
+            self._in_sets = [{}, {}]
+            self._in_free = [None, None]
+            self._in_next = 0
+        i = self._in_next
+        self._in_next ^= 1
+        dev_in = self._in_sets[i]
+        srcs = {"q": q, "k": k, "v": v, "h": h, "label_off": label_off, "label_ids": label_ids}
+        for name, src in srcs.items():
+            d = dev_in.get(name)
+            if d is None or d.numel() < src.numel() or d.dtype != src.dtype:
+                d = torch.empty(max(src.numel(), 1), dtype=src.dtype, device=self.device)
+                dev_in[name] = d
+        cs = self._copy_stream
+        if self._in_free[i] is not None:
+            cs.wait_event(self._in_free[i])  # the pass that read this set is done
+        views = {}
+        with torch.cuda.stream(cs):
+            for name, src in srcs.items():
+                view = dev_in[name][:src.numel()].view(src.shape)
+                view.copy_(src, non_blocking=True)
+                views[name] = view
+            copied = torch.cuda.Event()
+            copied.record(cs)
+        st.wait_event(copied)
+        res = self.run(req_of_branch, tok_offsets, tokens, views["q"], views["k"], views["v"],
+                       views["h"], W, views["label_off"], views["label_ids"], st.cuda_stream,
+                       schedule, qtype)
+        with torch.cuda.stream(st):
+            probs_out.copy_(res.probs, non_blocking=True)
+            argmax_out.copy_(res.argmax, non_blocking=True)
+            done = torch.cuda.Event()
+            done.record(st)
+        self._in_free[i] = done
+        return res
+
+    def _torch_stream(self, stream):
+        if stream is None:
+            return torch.cuda.current_stream(self.device)
+        if isinstance(stream, torch.cuda.Stream):
+            return stream
+        return torch.cuda.ExternalStream(int(stream), device=self.device)
+
     @property
     def last_launches(self) -> int:
         return (getattr(self, "last_attention_launches", 0) + getattr(self, "last_logprob_launches", 0)
