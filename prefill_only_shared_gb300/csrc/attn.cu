@@ -307,20 +307,29 @@ __device__ __forceinline__ void cursor_level(Cursor& c, const AttnArgs& a, const
     c.row0 = an.node_start;
     c.own = false;
     c.local = computed_here(a, an);
-  } else {
+  } else if (c.level == sd.chain_len) {
     c.len = td.t0 + td.nt;
     c.n_pages = (sd.len + kPageSize - 1) / kPageSize;
     c.page_off = sd.page_off;
     c.row0 = sd.node_start;
     c.own = true;
     c.local = computed_here(a, sd);
+  } else {  // a paired tile's second own level: the sibling leaf of half B
+    const SegDesc s2 = a.segs[td.seg2];
+    c.len = td.t0b + td.ntb;
+    c.n_pages = (s2.len + kPageSize - 1) / kPageSize;
+    c.page_off = s2.page_off;
+    c.row0 = s2.node_start;
+    c.own = true;
+    c.local = computed_here(a, s2);
   }
   c.n_units = (c.len + kKeysPerUnit - 1) / kKeysPerUnit;
 }
 
 __device__ __forceinline__ void cursor_next(Cursor& c, const AttnArgs& a, const SegDesc& sd,
                                             const TileDesc& td) {
-  if (++c.j >= c.n_units && c.level < sd.chain_len) {
+  const int last = sd.chain_len + (td.seg2 >= 0 ? 1 : 0);
+  if (++c.j >= c.n_units && c.level < last) {
     c.level += 1;
     c.j = 0;
     cursor_level(c, a, sd, td);
@@ -400,7 +409,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_units = td.u_hi - td.u_lo;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.G;
-  const bool has_b = td.nt > kHalf / G;  // half B holds at least one token
+  // half B continues half A's tokens, or (a paired tile) holds the tail of
+  // a sibling leaf
+  const bool has_b = td.seg2 >= 0 || td.nt > kHalf / G;  // half B holds at least one token
 
   const int n_halves = has_b ? 2 : 1;
   if (threadIdx.x == 0) {
@@ -450,7 +461,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int h = 0; h < 2; ++h)
           for (int slab = 0; slab < D / 64; ++slab)
             tma_load_3d(sQ + h * C::kQHalf + slab * C::kQSlab, &tmQ, q_full, slab * 64, hkv * G,
-                        (int32_t)(sd.node_start + td.t0 + h * (kHalf / G)));
+                        (int32_t)(h == 0 ? sd.node_start + td.t0
+                                  : td.seg2 >= 0 ? a.segs[td.seg2].node_start + td.t0b
+                                                 : sd.node_start + td.t0 + kHalf / G));
       }
       if (!is_k && lane == 0) {
         prefetch_tensormap(&tmVr);
@@ -637,8 +650,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- softmax / epilogue of one half ----------------
     const int h = warp >> 2;
     const int r = threadIdx.x & 127;  // row within the half = TMEM lane
-    const int tok = h * (kHalf / G) + r / G;
-    const int token = td.t0 + tok;    // position within the own segment
+    const int tok = r / G;  // token within the half
+    // the row's position within its half's segment
+    const int token = (h == 0 ? td.t0 : td.seg2 >= 0 ? td.t0b : td.t0 + kHalf / G) + tok;
     const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     const uint32_t s_col = C::kColS + (uint32_t)(h * kKeysPerUnit);
     const uint32_t o_col = C::kColO + (uint32_t)(h * D);
@@ -659,7 +673,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // visible keys of this row in this unit: c < lim
       const int key0 = walk.cur.j * kKeysPerUnit;
       int lim = walk.cur.len - key0;
-      if (walk.cur.own) lim = min(lim, token - key0 + 1);
+      if (walk.cur.own) {
+        // a paired tile's own levels: half A's segment, then half B's; each
+        // half sees only its own (causally)
+        const bool other = td.seg2 >= 0 && ((walk.cur.level > sd.chain_len) != (h == 1));
+        lim = other ? 0 : min(lim, token - key0 + 1);
+      }
       if (__any_sync(0xffffffffu, lim < kKeysPerUnit)) {
 #pragma unroll
         for (int c = 0; c < kKeysPerUnit; ++c) sv[c] = c < lim ? sv[c] : -INFINITY;
@@ -722,14 +741,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const float lse = l > 0.f ? (m_used + __log2f(l)) * 0.69314718055994531f : -INFINITY;
-      const bool row_ok = tok < td.nt;
+      // half h's rows: tokens of its segment from seg_row0 on, nt_h of them
+      const bool pair_b = h == 1 && td.seg2 >= 0;
+      const int nt_h = h == 0 ? min(td.nt, kHalf / G) : pair_b ? td.ntb : td.nt - kHalf / G;
+      const int64_t seg_row0 = pair_b ? a.segs[td.seg2].node_start : sd.node_start;
+      const bool row_ok = tok < nt_h;
       const int head = hkv * G + (r % G);
-      const size_t orow = (size_t)(sd.node_start + token) * a.Hq + head;
+      const size_t orow = (size_t)(seg_row0 + token) * a.Hq + head;
       const size_t prow_i = ((size_t)td.part * a.Hkv + hkv) * kRowsPerTile + h * kHalf + r;
       // A final half whose rows are all tokens of the tile goes out through
       // the Q_h buffer (its products are done) and TMA stores: rows laid out
       // like the Q box (token x head), 128-byte swizzled.
-      const bool staged = td.part < 0 && (h + 1) * (kHalf / G) <= td.nt;
+      const bool staged = td.part < 0 && nt_h >= kHalf / G;
       unsigned char* stage = sQ + h * C::kQHalf;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
@@ -777,7 +800,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (mbar_wait(&stage_full[h], 0, abort_flag)) {
             for (int slab = 0; slab < D / 64; ++slab)
               tma_store_3d(&tmO, stage + slab * C::kQSlab, slab * 64, hkv * G,
-                           (int32_t)(sd.node_start + td.t0 + h * (kHalf / G)));
+                           (int32_t)(seg_row0 + token - tok));
             bulk_commit_and_wait_read();  // the smem stays valid until the stores read it
           } else {
             if (!*abort_flag) raise_error(a.err, kErrTimeout);

@@ -33,9 +33,15 @@ struct SegDesc {
 // to the causal bound).  part < 0: write final out/lse; else write partial
 // slot `part`, which the call's merge entry `merge` combines with the other
 // parts of the split tile.
+// A paired tile (seg2 >= 0) holds the last tokens of two sibling leaves, each
+// fitting one 128-row half: half A tokens [t0, t0+nt) of `seg`, half B tokens
+// [t0b, t0b+ntb) of `seg2`.  Both read the common ancestors; then come the
+// own units of `seg` (half A's) and of `seg2` (half B's), each half masking
+// the other's.  Paired tiles are never split.
 struct TileDesc {
   int32_t seg, t0, nt, u_lo, u_hi, part;
-  int32_t merge, pad1;
+  int32_t merge, seg2, t0b, ntb;
+  int32_t pad0, pad1;
 };
 
 // Rows of one split tile whose `nparts` partials start at slot part0.

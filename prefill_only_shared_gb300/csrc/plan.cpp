@@ -461,7 +461,11 @@ sp_status build(const sp_shape* shape, sp_cache* cache, int32_t n_branches,
     const bool all = r == n_rounds;
     for (int kind = 0; kind < sp_plan::kCallKinds; ++kind) {
       sp_plan::Call& call = P->calls[(size_t)sp_plan::kCallKinds * r + kind];
-      struct Raw { int32_t seg, t0, nt; int64_t units; };
+      struct Raw {
+        int32_t seg, t0, nt;
+        int64_t units;
+        int32_t seg2, t0b, ntb;  // a paired sibling tail (seg2 >= 0)
+      };
       std::vector<Raw> raw;
       call.append_off = (int64_t)appends.size();
       for (int32_t s = 0; s < S; ++s) {
@@ -472,7 +476,7 @@ sp_status build(const sp_shape* shape, sp_cache* cache, int32_t n_branches,
             appends.push_back({s, pg});
         for (int32_t t0 = 0; t0 < P->seg_len[s]; t0 += TPT) {
           int32_t nt = std::min(TPT, P->seg_len[s] - t0);
-          raw.push_back({s, t0, nt, anc_units[s] + ceil_div(t0 + nt, sp::kKeysPerUnit)});
+          raw.push_back({s, t0, nt, anc_units[s] + ceil_div(t0 + nt, sp::kKeysPerUnit), -1, 0, 0});
         }
       }
       if (kind >= 1) {
@@ -482,20 +486,52 @@ sp_status build(const sp_shape* shape, sp_cache* cache, int32_t n_branches,
           if (!P->branch_recompute[b]) continue;
           int32_t s = P->branch_last_seg[b];
           int32_t t0 = P->seg_len[s] - 1;
-          raw.push_back({s, t0, 1, anc_units[s] + ceil_div(t0 + 1, sp::kKeysPerUnit)});
+          raw.push_back({s, t0, 1, anc_units[s] + ceil_div(t0 + 1, sp::kKeysPerUnit), -1, 0, 0});
         }
       }
       call.n_append = (int64_t)appends.size() - call.append_off;
       // When the call has fewer tiles than one wave of CTAs, split the long
       // tiles' KV walks into parts (merged afterwards) so the call fills the
       // GPU, keeping the total within one wave; then schedule longest first.
+      const bool split_mode = (int64_t)raw.size() < part_target;
+      // Otherwise pair the last tiles of sibling leaves whose tokens fit one
+      // 128-row half each: one CTA walks their common ancestors once, then
+      // both own segments (each half masking the other's), where two CTAs
+      // would each run one half alone.
+      if (!split_mode) {
+        const int32_t half = TPT / 2;
+        std::map<int32_t, size_t> open;  // parent segment -> an unpaired tail
+        std::vector<char> drop(raw.size(), 0);
+        for (size_t i = 0; i < raw.size(); ++i) {
+          const Raw& x = raw[i];
+          const int32_t par = P->seg_parent[x.seg];
+          if (P->seg_shared[x.seg] || par < 0 || x.nt > half || x.t0 + x.nt != P->seg_len[x.seg])
+            continue;
+          auto it = open.find(par);
+          if (it == open.end()) {
+            open[par] = i;
+            continue;
+          }
+          Raw& y = raw[it->second];
+          y.seg2 = x.seg;
+          y.t0b = x.t0;
+          y.ntb = x.nt;
+          y.units += ceil_div(x.t0 + x.nt, sp::kKeysPerUnit);  // x's own units
+          drop[i] = 1;
+          open.erase(it);
+        }
+        size_t w = 0;
+        for (size_t i = 0; i < raw.size(); ++i)
+          if (!drop[i]) raw[w++] = raw[i];
+        raw.resize(w);
+      }
       int64_t total_units = 0, max_units = 0;
       for (auto& x : raw) {
         total_units += x.units;
         max_units = std::max<int64_t>(max_units, x.units);
       }
       int64_t budget = std::max<int64_t>(max_units, 1);  // no split
-      if ((int64_t)raw.size() < part_target) {
+      if (split_mode) {
         budget = std::max<int64_t>(kMinUnitsPerPart, ceil_div(std::max<int64_t>(total_units, 1), part_target));
         auto n_ctas = [&](int64_t b) {
           int64_t n = 0;
@@ -510,7 +546,8 @@ sp_status build(const sp_shape* shape, sp_cache* cache, int32_t n_branches,
       int32_t parts = 0;
       for (auto& x : raw) {
         if (x.units <= budget) {
-          work.push_back({{x.seg, x.t0, x.nt, 0, (int32_t)x.units, -1, -1, 0}, x.units});
+          work.push_back({{x.seg, x.t0, x.nt, 0, (int32_t)x.units, -1, -1, x.seg2, x.t0b, x.ntb, 0, 0},
+                          x.units});
           continue;
         }
         int32_t np = (int32_t)ceil_div(x.units, budget);
@@ -518,7 +555,7 @@ sp_status build(const sp_shape* shape, sp_cache* cache, int32_t n_branches,
         merges.push_back({x.seg, x.t0, x.nt, parts, np, 0, 0, 0});
         for (int32_t i = 0; i < np; ++i) {
           int32_t lo = (int32_t)(x.units * i / np), hi = (int32_t)(x.units * (i + 1) / np);
-          work.push_back({{x.seg, x.t0, x.nt, lo, hi, parts + i, mi, 0}, (int64_t)(hi - lo)});
+          work.push_back({{x.seg, x.t0, x.nt, lo, hi, parts + i, mi, -1, 0, 0, 0, 0}, (int64_t)(hi - lo)});
         }
         parts += np;
       }

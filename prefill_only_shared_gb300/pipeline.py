@@ -50,6 +50,9 @@ class SharedPrefixClassifier:
             max_pages = int(prefix_cache_pages)
         self.fixed_pool = max_pages is not None
         self.n_sms = torch.cuda.get_device_properties(self.device).multi_processor_count
+        # SMs the planner sizes attention calls for (splits of small calls,
+        # pairing of leaf tails); the device's count unless set
+        self.plan_sms = None
         self._bufs = {}
         self._views = {}
         self._lm_ws_key = None
@@ -97,9 +100,9 @@ class SharedPrefixClassifier:
         uncached remainders: q / k / v rows exist for those alone."""
         if self.cache is not None:
             return sp.sp_plan_build_cached(self.shape, self.cache, req_of_branch, tok_offsets,
-                                           tokens, self.n_sms)
+                                           tokens, self.plan_sms or self.n_sms)
         plan = sp.sp_plan_build(self.shape, req_of_branch, tok_offsets, tokens, self.max_pages,
-                                self.n_sms)
+                                self.plan_sms or self.n_sms)
         self._ensure_pool(plan.stats()["pages_used"])
         return plan
 

@@ -21,13 +21,17 @@ TOL_P = 1e-3
 ARGMAX_MARGIN = 1e-2
 
 
-def run_gpu(wl, stream=None, schedule="rounds"):
+def run_gpu(wl, stream=None, schedule="rounds", n_sms=None):
+    """n_sms: plan for that many SMs (small values turn split parts off and
+    the pairing of sibling leaf tails on)."""
     from prefill_only_shared_gb300 import sp
     from prefill_only_shared_gb300.pipeline import SharedPrefixClassifier
     dev = torch.device("cuda:0")
     sh = wl.shape
     clf = SharedPrefixClassifier(sh.n_q_heads, sh.n_kv_heads, sh.head_dim, sh.hidden, sh.vocab,
                                  device=dev)
+    if n_sms is not None:
+        clf.plan_sms = n_sms
     q, k, v = wl.q.to(dev), wl.k.to(dev), wl.v.to(dev)
     h, W = wl.h.to(dev), wl.W.to(dev)
     off = torch.from_numpy(wl.label_off).to(dev)

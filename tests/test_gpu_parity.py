@@ -54,6 +54,25 @@ def test_small_ragged_cases(cuda_dev, lib, case, schedule):
     check_readout(wl, g)
 
 
+@pytest.mark.parametrize("schedule", ["rounds", "tree"])
+@pytest.mark.parametrize("case", range(len(SMALL)))
+def test_small_cases_with_paired_tails(cuda_dev, lib, case, schedule):
+    """Planned for one SM: no split parts, and sibling leaf tails that fit a
+    half share a CTA (half A one leaf's tail, half B the other's)."""
+    import sys
+    sys.path.insert(0, __import__("os").path.dirname(__file__))
+    from test_plan_descriptor import decode
+    trees, Hq, Hkv, d, H, V, labels = SMALL[case]
+    wl = small_case(trees, seed=case, n_q_heads=Hq, n_kv_heads=Hkv, head_dim=d, hidden=H,
+                    vocab=V, labels=labels)
+    g = run_gpu(wl, schedule=schedule, n_sms=1)
+    check_attention_full(wl, g)
+    check_readout(wl, g)
+    tiles = decode(g["plan"].descriptor())[4]
+    if case in (0, 1, 3, 4):  # cases with sibling leaf tails short enough to pair
+        assert (tiles["seg2"] >= 0).any()
+
+
 def test_recomputed_final_rows(cuda_dev, lib):
     """Branches equal to, or prefixes of, other branches: their last row is
     cached before their round and is recomputed (same value)."""

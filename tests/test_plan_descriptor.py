@@ -22,7 +22,8 @@ from test_oracle_staging import csr, random_case
 SEG = np.dtype([("node_start", "<i8"), ("len", "<i4"), ("page_off", "<i4"), ("chain_off", "<i4"),
                 ("chain_len", "<i4"), ("round", "<i4"), ("shared", "<i4")])
 TILE = np.dtype([("seg", "<i4"), ("t0", "<i4"), ("nt", "<i4"), ("u_lo", "<i4"), ("u_hi", "<i4"),
-                 ("part", "<i4"), ("merge", "<i4"), ("p1", "<i4")])
+                 ("part", "<i4"), ("merge", "<i4"), ("seg2", "<i4"), ("t0b", "<i4"), ("ntb", "<i4"),
+                 ("p0", "<i4"), ("p1", "<i4")])
 MERGE = np.dtype([("seg", "<i4"), ("t0", "<i4"), ("nt", "<i4"), ("part0", "<i4"), ("nparts", "<i4"),
                   ("p0", "<i4"), ("p1", "<i4"), ("p2", "<i4")])
 APP = np.dtype([("seg", "<i4"), ("page", "<i4")])
@@ -73,8 +74,58 @@ def emulate(plan, q, k, v, Hq, Hkv, d, schedule="rounds", pool=None):
                           for p in range((x["len"] + PAGE - 1) // PAGE))
             assert sorted((int(a["seg"]), int(a["page"])) for a in apps) == want
             parts = {}
+
+            def attend_rows(seg, t0, nt, keys):
+                for tok in range(nt):
+                    row = seg["node_start"] + t0 + tok
+                    seen[row] += 1
+                    vis = [kv for kv in keys if kv[2] <= t0 + tok]
+                    for hq in range(Hq):
+                        g = hq // G
+                        sc = np.array([kk[0][g] @ q[row, hq] for kk in vis]) * scale
+                        m = sc.max()
+                        pr = np.exp(sc - m)
+                        out[row, hq] = (pr @ np.array([kk[1][g] for kk in vis])) / pr.sum()
+                        lse[row, hq] = m + math.log(pr.sum())
+
+            def level_keys(x, ln, own):
+                ks = []
+                for pos in range(ln):
+                    if in_call(x):
+                        kk, vv = k[x["node_start"] + pos], v[x["node_start"] + pos]
+                    else:
+                        pg = pages[x["page_off"] + pos // PAGE]
+                        kk, vv = pool[pg, 0, :, pos % PAGE], pool[pg, 1, :, pos % PAGE]
+                    ks.append((kk, vv, pos if own else -1))
+                return ks
+
+            def paired_tile(td, in_call):
+                # two sibling leaves' last tokens, each in one half: common
+                # ancestors, then each half's own segment (never split)
+                sa, sb = segs[td["seg"]], segs[td["seg2"]]
+                assert td["part"] < 0 and td["merge"] == -1 and td["u_lo"] == 0
+                assert sa["shared"] == 0 and sb["shared"] == 0 and td["nt"] <= ROWS // 2 // G
+                assert td["ntb"] <= ROWS // 2 // G
+                assert td["t0"] + td["nt"] == sa["len"] and td["t0b"] + td["ntb"] == sb["len"]
+                ca = chain[sa["chain_off"]:sa["chain_off"] + sa["chain_len"]]
+                cb = chain[sb["chain_off"]:sb["chain_off"] + sb["chain_len"]]
+                assert list(ca) == list(cb) and len(ca) > 0
+                anc = []
+                n_units = 0
+                for c in ca:
+                    x = segs[c]
+                    anc += level_keys(x, x["len"], False)
+                    n_units += (x["len"] + UNIT - 1) // UNIT
+                n_units += (sa["len"] + UNIT - 1) // UNIT + (sb["len"] + UNIT - 1) // UNIT
+                assert td["u_hi"] == n_units
+                attend_rows(sa, td["t0"], td["nt"], anc + level_keys(sa, sa["len"], True))
+                attend_rows(sb, td["t0b"], td["ntb"], anc + level_keys(sb, sb["len"], True))
+
             call_merges = merges[ci["merge_off"]:ci["merge_off"] + ci["n_merges"]]
             for td in tiles[ci["tile_off"]:ci["tile_off"] + ci["n_tiles"]]:
+                if td["seg2"] >= 0:
+                    paired_tile(td, in_call)
+                    continue
                 s = segs[td["seg"]]
                 if td["part"] >= 0:  # a split part names its merge entry
                     md = call_merges[td["merge"]]
@@ -165,8 +216,13 @@ def test_descriptor_tree_cases(lib, n_sms, G, Hkv):
     trees = [(130, [(70, [(3, []), (65, []), (1, [])]), (17, [])]), (40, []),
              (5, [(1, []), (200, [])])]
     wl = small_case(trees, n_q_heads=G * Hkv, n_kv_heads=Hkv, head_dim=64)
-    check(wl.req_of_branch, wl.tok_offsets, wl.tokens, A.to64(wl.q), A.to64(wl.k), A.to64(wl.v),
-          G * Hkv, Hkv, 64, lib, n_sms)
+    plan = check(wl.req_of_branch, wl.tok_offsets, wl.tokens, A.to64(wl.q), A.to64(wl.k),
+                 A.to64(wl.v), G * Hkv, Hkv, 64, lib, n_sms)
+    if n_sms == 1:  # calls of a wave or more: sibling leaf tails share CTAs
+        tiles = decode(plan.descriptor())[4]
+        ci = plan.call_info(-1, 2)
+        tree_tiles = tiles[ci["tile_off"]:ci["tile_off"] + ci["n_tiles"]]
+        assert (tree_tiles["seg2"] >= 0).sum() >= 1
 
 
 @pytest.mark.parametrize("seed", range(12))
