@@ -89,9 +89,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* dyn_count = unit_ring + kUnitRing;                  // labels of the shared tail's rows
   float2* state = reinterpret_cast<float2*>(tmem_slot + 8);  // [4][N]
   // labels whose id falls in this CTA's vocab rows (indices into label_ids),
-  // the branch of every label j < lab_cap, and the list length
+  // with their ids (so a tile's scan stays in shared memory), the branch of
+  // every label j < lab_cap, and the list length
   int32_t* lab_list = reinterpret_cast<int32_t*>(state + 4 * a.N);     // [lab_cap]
-  uint16_t* lab_br = reinterpret_cast<uint16_t*>(lab_list + a.lab_cap);  // [lab_cap]
+  int32_t* lab_id = lab_list + a.lab_cap;                               // [lab_cap]
+  uint16_t* lab_br = reinterpret_cast<uint16_t*>(lab_id + a.lab_cap);   // [lab_cap]
   int* lab_count = reinterpret_cast<int*>(lab_br + ((a.lab_cap + 1) & ~1));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -251,15 +253,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int v_lo = (u_begin / a.n_ch) * kVT;
       const int v_hi = u_end > u_begin ? ((u_end - 1) / a.n_ch + 1) * kVT : v_lo;
       const int t_lo = (tail_lo / a.n_ch) * kVT;
-      for (int j = threadIdx.x - 64; j < a.n_labels; j += 128) {
-        const int id = a.label_ids[j];
-        if (id >= v_lo && id < v_hi) {
-          const int k = atomicAdd(lab_count, 1);
-          if (k < a.lab_cap) lab_list[k] = j;
+      // one shared-memory atomic per warp and list (ballot, then each lane
+      // takes its rank among the warp's matches)
+      const unsigned below = (1u << lane) - 1u;
+      for (int j0 = (warp - 2) * 32; j0 < a.n_labels; j0 += 128) {
+        const int j = j0 + lane;
+        const int id = j < a.n_labels ? a.label_ids[j] : -1;
+        const bool in_run = id >= v_lo && id < v_hi;
+        const bool in_tail = id >= t_lo && tail_lo < a.n_units;
+        const unsigned m_run = __ballot_sync(0xffffffffu, in_run);
+        const unsigned m_tail = __ballot_sync(0xffffffffu, in_tail);
+        int b_run = 0, b_tail = 0;
+        if (lane == 0) {
+          if (m_run) b_run = atomicAdd(lab_count, __popc(m_run));
+          if (m_tail) b_tail = atomicAdd(dyn_count, __popc(m_tail));
         }
-        if (id >= t_lo && tail_lo < a.n_units) {
-          const int k = atomicAdd(dyn_count, 1);
-          if (k < a.lab_cap) lab_list[a.lab_cap - 1 - k] = j;
+        b_run = __shfl_sync(0xffffffffu, b_run, 0);
+        b_tail = __shfl_sync(0xffffffffu, b_tail, 0);
+        if (in_run) {
+          const int k = b_run + __popc(m_run & below);
+          if (k < a.lab_cap) {
+            lab_list[k] = j;
+            lab_id[k] = id;
+          }
+        }
+        if (in_tail) {
+          const int k = b_tail + __popc(m_tail & below);
+          if (k < a.lab_cap) {
+            lab_list[a.lab_cap - 1 - k] = j;
+            lab_id[a.lab_cap - 1 - k] = id;
+          }
         }
       }
       asm volatile("bar.sync 1, 128;" ::: "memory");
@@ -322,8 +345,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int j_hi = use_list ? n_local : a.label_off[n_hi];
       for (int jb = j_lo; jb < j_hi; jb += 32) {
         const int e = jb + lane;
-        const int j = e < j_hi ? (use_list ? lab_list[in_tail ? a.lab_cap - 1 - e : e] : e) : -1;
-        const int id = j >= 0 ? a.label_ids[j] : -1;
+        const int slot = in_tail ? a.lab_cap - 1 - e : e;
+        const int j = e < j_hi ? (use_list ? lab_list[slot] : e) : -1;
+        const int id = j < 0 ? -1 : use_list ? lab_id[slot] : a.label_ids[j];
         bool match = id >= v_base && id < v_base + 32 && id < a.V;
         int br = -1;
         if (match) {
@@ -447,9 +471,9 @@ Geometry geometry(int N, int V, int n_sms, int n_labels = 0) {
                           ? kSmemCap - base - (size_t)st_keep * stage
                           : 0;
   int lab = n_labels < kLabelCache ? n_labels : kLabelCache;
-  if ((size_t)lab * 6 + 32 > room) lab = room > 32 ? (int)((room - 32) / 6) : 0;
+  if ((size_t)lab * 10 + 32 > room) lab = room > 32 ? (int)((room - 32) / 10) : 0;
   g.lab_cap = lab;
-  const size_t fixed = base + (size_t)g.lab_cap * 6 + 32;
+  const size_t fixed = base + (size_t)g.lab_cap * 10 + 32;
   int st = (int)((kSmemCap - fixed) / stage);
   if (st > kMaxStages) st = kMaxStages;
   g.stages = st;
