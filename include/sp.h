@@ -493,6 +493,40 @@ sp_status sp_option_softmax(const float* row_logprobs, int32_t n_rows, const int
                             const float* prior, float* scores, float* probs, int32_t* argmax,
                             void* stream);
 
+/* One whole pass of the path in one call: sp_plan_build over the branches,
+ * sp_plan_upload, one sp_tree_attn call for the whole trie (SP_ALL_ROUNDS),
+ * sp_label_logprobs and sp_label_softmax, all enqueued on `stream` (the
+ * openjev-sglang article's request flow: shared prefix and branches prefilled,
+ * label log-probabilities read at each branch's last position, renormalised).
+ * For callers that drive the path from C, or want its host work in one call.
+ *   HOST    req_of_branch, tok_offsets, tokens: as for sp_plan_build
+ *   DEVICE  q, k, v: node_rows rows in the plan's node-token order (the order
+ *           sp_plan_build documents; node_rows must equal its node tokens)
+ *           kv_pool: pool_pages pages; out, lse: node_rows rows
+ *           desc: desc_bytes, 256-byte aligned; attn_ws: attn_ws_bytes
+ *           h [n_branches, shape->hidden], W [shape->vocab, shape->hidden],
+ *           label_off [n_branches+1], label_ids [n_labels], logprobs and
+ *           probs [n_labels], lse_vocab and argmax [n_branches],
+ *           lm_ws: lm_ws_bytes (sp_label_workspace_bytes(n_branches, vocab, 0))
+ *   stats   HOST, may be NULL: the pass's plan statistics, filled whenever
+ *           the plan was built (also on SP_ERR_WORKSPACE and SP_ERR_POOL_FULL,
+ *           where pages_used gives the pool size needed)
+ * Every capacity is checked before the first launch: SP_ERR_POOL_FULL when
+ * the plan needs more than pool_pages pages, SP_ERR_WORKSPACE when desc_bytes,
+ * attn_ws_bytes or lm_ws_bytes is short (stats gives desc_bytes and
+ * attn_workspace_bytes; nothing is launched then), SP_ERR_ARG when node_rows
+ * differs from the plan's node tokens; other errors as for the calls it
+ * makes.  The plan lives only inside the call (the descriptor upload stages
+ * it out of host memory before returning). */
+sp_status sp_run_pass(const sp_shape* shape, int32_t n_branches, const int32_t* req_of_branch,
+                      const int64_t* tok_offsets, const int32_t* tokens, int64_t node_rows,
+                      const void* q, const void* k, const void* v, void* kv_pool,
+                      int32_t pool_pages, void* out, float* lse, void* desc, size_t desc_bytes,
+                      void* attn_ws, size_t attn_ws_bytes, const void* h, const void* W,
+                      const int32_t* label_off, const int32_t* label_ids, int32_t n_labels,
+                      float* logprobs, float* lse_vocab, void* lm_ws, size_t lm_ws_bytes,
+                      float* probs, int32_t* argmax, void* stream, sp_plan_stats* stats);
+
 /* Host-side validation of the option CSRs of sp_option_softmax (HOST
  * arrays): opt_off starts at 0, increases strictly and ends <= n_rows; q_off
  * starts at 0, ends <= n_opts, and gives every question 2..64 options.

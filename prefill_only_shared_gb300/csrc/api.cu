@@ -1,6 +1,7 @@
 // C-ABI entry points that touch the GPU: descriptor upload, the two
 // attention calls, the label readout and softmax, and the device error word.
 // Every argument is validated on the host before anything is launched.
+#include <climits>
 #include <cstring>
 #include <mutex>
 
@@ -359,6 +360,59 @@ extern "C" sp_status sp_option_softmax(const float* row_logprobs, int32_t n_rows
                                          n_questions, prior, scores, probs, argmax, err, stream);
   t_last_launches = 1;
   return e == cudaSuccess ? SP_OK : SP_ERR_CUDA;
+}
+
+extern "C" sp_status sp_run_pass(const sp_shape* shape, int32_t n_branches,
+                                   const int32_t* req_of_branch, const int64_t* tok_offsets,
+                                   const int32_t* tokens, int64_t node_rows, const void* q,
+                                   const void* k, const void* v, void* kv_pool, int32_t pool_pages,
+                                   void* out, float* lse, void* desc, size_t desc_bytes,
+                                   void* attn_ws, size_t attn_ws_bytes, const void* h,
+                                   const void* W, const int32_t* label_off,
+                                   const int32_t* label_ids, int32_t n_labels, float* logprobs,
+                                   float* lse_vocab, void* lm_ws, size_t lm_ws_bytes,
+                                   float* probs, int32_t* argmax, void* stream,
+                                   sp_plan_stats* stats) {
+  t_last_launches = 0;
+  if (!shape || !probs || !argmax) return SP_ERR_ARG;
+  sp_plan* plan = nullptr;
+  // planned without a page limit, so that a pool that is too small still
+  // reports the pages needed
+  sp_status st = sp_plan_build(shape, n_branches, req_of_branch, tok_offsets, tokens, INT32_MAX,
+                               sm_count(), &plan);
+  if (st != SP_OK) return st;
+  sp_plan_stats ps;
+  sp_plan_get_stats(plan, &ps);
+  if (stats) *stats = ps;
+  // every capacity is checked before the first launch
+  const size_t lm_need =
+      sp::lmhead_workspace_bytes(n_branches, shape->vocab, sm_count());
+  if (ps.node_tokens != node_rows) st = SP_ERR_ARG;
+  else if (ps.pages_used > pool_pages) st = SP_ERR_POOL_FULL;
+  else if ((size_t)ps.desc_bytes > desc_bytes || (size_t)ps.attn_workspace_bytes > attn_ws_bytes ||
+           lm_ws_bytes < lm_need)
+    st = SP_ERR_WORKSPACE;
+  int32_t launches = 0;
+  if (st == SP_OK) st = sp_plan_upload(plan, desc, desc_bytes, stream);
+  if (st == SP_OK) {
+    st = sp_tree_attn(plan, desc, SP_ALL_ROUNDS, q, k, v, kv_pool, out, lse, attn_ws,
+                      attn_ws_bytes, stream);
+    launches += t_last_launches;
+  }
+  // the upload staged the descriptor out of the plan's (pageable) memory
+  // before returning, so the plan can go
+  sp_plan_free(plan);
+  if (st == SP_OK) {
+    st = sp_label_logprobs(h, W, n_branches, shape->hidden, shape->vocab, label_off, label_ids,
+                           n_labels, logprobs, lse_vocab, lm_ws, lm_ws_bytes, stream);
+    launches += t_last_launches;
+  }
+  if (st == SP_OK) {
+    st = sp_label_softmax(logprobs, label_off, n_branches, probs, argmax, stream);
+    launches += t_last_launches;
+  }
+  t_last_launches = launches;
+  return st;
 }
 
 extern "C" sp_status sp_wait_flag(const uint32_t* flag, uint32_t expect, int64_t limit_ns,

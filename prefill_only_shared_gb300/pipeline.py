@@ -25,7 +25,7 @@ class PassOutputs:
     lse_vocab: torch.Tensor  # fp32 [N]
     probs: torch.Tensor  # fp32 [n_labels]
     argmax: torch.Tensor  # int32 [N]
-    plan: "sp.Plan"
+    plan: "sp.Plan | None"  # None from run_pass (the plan lives inside the native call)
     value: torch.Tensor | None = None  # fp32 [N], with question types
     confidence: torch.Tensor | None = None  # fp32 [N], with question types
 
@@ -249,6 +249,53 @@ class SharedPrefixClassifier:
             h, W, label_off, label_ids, n_labels, stream, qtype)
         return PassOutputs(out, lse, logprobs, lse_v, probs, argmax, plan, value, conf)
 
+    def run_pass(self, req_of_branch, tok_offsets, tokens, q, k, v, h, W, label_off, label_ids,
+                 stream=None) -> PassOutputs:
+        """The whole pass in one native call (sp_run_pass: plan, upload, one
+        tree attention call, readout, softmax), so the host work is the C++
+        planner's.  Buffers grow when the call reports SP_ERR_WORKSPACE or
+        SP_ERR_POOL_FULL (nothing is launched then) and the call is repeated.
+        Not with a prefix cache (its plans come from sp_plan_build_cached)."""
+        if self.cache is not None:
+            raise ValueError("run_pass plans without the prefix cache")
+        stream = self._stream(stream)
+        s = self.shape
+        T, N, nl = int(q.shape[0]), int(h.shape[0]), int(label_ids.numel())
+        out = self._buf("out", T * s.n_q_heads * s.head_dim, torch.bfloat16).view(
+            T, s.n_q_heads, s.head_dim)
+        lse = self._buf("lse", T * s.n_q_heads, torch.float32).view(T, s.n_q_heads)
+        logprobs = self._buf("logprobs", nl, torch.float32)
+        lse_v = self._buf("lse_vocab", N, torch.float32)
+        probs = self._buf("probs", nl, torch.float32)
+        argmax = self._buf("argmax", N, torch.int32)
+        wkey = (N, W.shape[0])
+        if self._lm_ws_key != wkey:
+            self._lm_ws_bytes = sp.sp_label_workspace_bytes(N, W.shape[0], self.n_sms)
+            self._lm_ws_key = wkey
+        lm_ws = self._buf("lm_ws", self._lm_ws_bytes, torch.uint8)
+        if not hasattr(self, "_pass_need"):
+            self._pass_need = {"desc_bytes": 4096, "attn_workspace_bytes": 0}
+        for _ in range(3):
+            need = self._pass_need
+            desc = self._desc_view(need["desc_bytes"])
+            ws = self._buf("attn_ws", need["attn_workspace_bytes"], torch.uint8)
+            status, st = sp.sp_run_pass(self.shape, req_of_branch, tok_offsets, tokens, q, k, v,
+                                        self.kv_pool, out, lse, desc, ws, h, W, label_off,
+                                        label_ids, logprobs, lse_v, lm_ws, probs, argmax, stream)
+            if status == sp.SP_OK:
+                break
+            need["desc_bytes"] = max(need["desc_bytes"], st["desc_bytes"])
+            need["attn_workspace_bytes"] = max(need["attn_workspace_bytes"],
+                                               st["attn_workspace_bytes"])
+            if status == 3:  # SP_ERR_POOL_FULL
+                if self.fixed_pool:
+                    raise sp.SpError(status, "sp_run_pass")
+                self._ensure_pool(st["pages_used"])
+        else:
+            raise sp.SpError(status, "sp_run_pass")
+        self.last_pass_launches = sp.sp_last_launch_count()
+        return PassOutputs(out, lse, logprobs, lse_v, probs, argmax, None)
+
     def run_from_host(self, req_of_branch, tok_offsets, tokens, q, k, v, h, W, label_off,
                       label_ids, probs_out, argmax_out, stream=None, schedule="rounds",
                       qtype=None) -> PassOutputs:
@@ -287,9 +334,14 @@ class SharedPrefixClassifier:
             copied = torch.cuda.Event()
             copied.record(cs)
         st.wait_event(copied)
-        res = self.run(req_of_branch, tok_offsets, tokens, views["q"], views["k"], views["v"],
-                       views["h"], W, views["label_off"], views["label_ids"], st.cuda_stream,
-                       schedule, qtype)
+        if schedule == "tree" and qtype is None and self.cache is None:
+            res = self.run_pass(req_of_branch, tok_offsets, tokens, views["q"], views["k"],
+                                views["v"], views["h"], W, views["label_off"],
+                                views["label_ids"], st.cuda_stream)
+        else:
+            res = self.run(req_of_branch, tok_offsets, tokens, views["q"], views["k"], views["v"],
+                           views["h"], W, views["label_off"], views["label_ids"], st.cuda_stream,
+                           schedule, qtype)
         with torch.cuda.stream(st):
             probs_out.copy_(res.probs, non_blocking=True)
             argmax_out.copy_(res.argmax, non_blocking=True)

@@ -93,6 +93,9 @@ SIGNATURES = {
     "sp_wait_flag": (_I32, [_P, ctypes.c_uint32, ctypes.c_int64, _P]),
     "sp_check_labels": (_I32, [_I32P, _I32P, _I32, _I32]),
     "sp_option_softmax": (_I32, [_P, _I32, _P, _I32, _P, _I32, _P, _P, _P, _P, _P]),
+    "sp_run_pass": (_I32, [ctypes.POINTER(sp_shape), _I32, _I32P, _I64P, _I32P, ctypes.c_int64,
+                           _P, _P, _P, _P, _I32, _P, _P, _P, _SZ, _P, _SZ, _P, _P, _P, _P, _I32,
+                           _P, _P, _P, _SZ, _P, _P, _P, ctypes.POINTER(sp_plan_stats)]),
     "sp_check_options": (_I32, [_I32P, _I32, _I32, _I32P, _I32]),
     "sp_check_device_error": (_I32, [_P]),
     "sp_status_str": (ctypes.c_char_p, [_I32]),
@@ -482,6 +485,36 @@ def sp_option_softmax(row_logprobs, opt_off, q_off, scores, probs, argmax, prior
         _dev(scores, torch.float32, "scores"), _dev(probs, torch.float32, "probs"),
         _dev(argmax, torch.int32, "argmax"), _stream(stream))
     _check(st, "sp_option_softmax")
+
+
+def sp_run_pass(shape: sp_shape, req_of_branch, tok_offsets, tokens, q, k, v, kv_pool, out,
+                lse, desc, attn_ws, h, W, label_off, label_ids, logprobs, lse_vocab, lm_ws, probs,
+                argmax, stream=None):
+    """One whole pass (plan, upload, tree attention, readout, softmax) in one
+    call.  Returns (status, plan stats dict): SP_ERR_WORKSPACE and
+    SP_ERR_POOL_FULL come back with the stats (nothing launched) so the
+    caller can grow its buffers and call again; other errors raise."""
+    req = _np(req_of_branch, np.int32)
+    off = _np(tok_offsets, np.int64)
+    tok = _np(tokens, np.int32)
+    st = sp_plan_stats()
+    status = lib().sp_run_pass(
+        ctypes.byref(shape), len(req), req.ctypes.data_as(_I32P), off.ctypes.data_as(_I64P),
+        tok.ctypes.data_as(_I32P), int(q.shape[0]), _dev(q, torch.bfloat16, "q"),
+        _dev(k, torch.bfloat16, "k"), _dev(v, torch.bfloat16, "v"),
+        _dev(kv_pool, torch.bfloat16, "kv_pool"), int(kv_pool.shape[0]),
+        _dev(out, torch.bfloat16, "out"), _dev(lse, torch.float32, "lse"),
+        _dev(desc, torch.uint8, "desc"), desc.numel(),
+        _dev(attn_ws, torch.uint8, "attn_ws") if attn_ws.numel() else None, attn_ws.numel(),
+        _dev(h, torch.bfloat16, "h"), _dev(W, torch.bfloat16, "W"),
+        _dev(label_off, torch.int32, "label_off"), _dev(label_ids, torch.int32, "label_ids"),
+        label_ids.numel(), _dev(logprobs, torch.float32, "logprobs"),
+        _dev(lse_vocab, torch.float32, "lse_vocab"), _dev(lm_ws, torch.uint8, "lm_ws"),
+        lm_ws.numel(), _dev(probs, torch.float32, "probs"), _dev(argmax, torch.int32, "argmax"),
+        _stream(stream), ctypes.byref(st))
+    if status not in (SP_OK, 3, 7):  # SP_ERR_POOL_FULL, SP_ERR_WORKSPACE: the caller grows
+        _check(status, "sp_run_pass")
+    return status, st.as_dict()
 
 
 def sp_check_options(opt_off, n_rows: int, q_off):

@@ -54,3 +54,41 @@ def test_host_input_passes_match_device_passes(cuda_dev, lib):
             x = np.sort(want[i][0][wl.label_off[n]:wl.label_off[n + 1]].numpy())[::-1]
             if x[0] - x[1] > 1e-4:
                 assert a[n] == want[i][1][n], (i, n)
+
+
+@pytest.mark.parametrize("name", ["tiny", "yesno", "choice64"])
+def test_native_pass_matches_the_orchestrated_pass(cuda_dev, lib, name):
+    """sp_run_pass (plan, upload, tree attention, readout and softmax in one
+    call) gives the results of the Python orchestration of the same calls;
+    its first call grows the descriptor and workspace buffers from the sizes
+    it reports."""
+    from prefill_only_shared_gb300 import sp
+    from prefill_only_shared_gb300.pipeline import SharedPrefixClassifier
+    from prefill_only_shared_gb300.workloads import make_workload
+    wl = make_workload(name, seed=0)
+    sh = wl.shape
+    dev = cuda_dev
+    args = (wl.req_of_branch, wl.tok_offsets, wl.tokens, wl.q.to(dev), wl.k.to(dev),
+            wl.v.to(dev), wl.h.to(dev), wl.W.to(dev), torch.from_numpy(wl.label_off).to(dev),
+            torch.from_numpy(wl.label_ids).to(dev))
+    ref = SharedPrefixClassifier(sh.n_q_heads, sh.n_kv_heads, sh.head_dim, sh.hidden, sh.vocab,
+                                 device=dev)
+    r = ref.run(*args, schedule="tree")
+    torch.cuda.synchronize()
+    want = {k: getattr(r, k).float().cpu().clone() for k in ("out", "lse", "probs")}
+    want_am = r.argmax.cpu().clone()
+    nat = SharedPrefixClassifier(sh.n_q_heads, sh.n_kv_heads, sh.head_dim, sh.hidden, sh.vocab,
+                                 device=dev)
+    for _ in range(2):  # the first call grows the buffers, the second reuses them
+        g = nat.run_pass(*args)
+        torch.cuda.synchronize()
+        sp.sp_check_device_error()
+        assert nat.last_pass_launches >= 3
+        assert torch.equal(g.out.float().cpu(), want["out"])
+        assert torch.equal(g.lse.cpu(), want["lse"])
+        assert (g.probs.cpu() - want["probs"]).abs().max().item() <= 1e-6
+        p = want["probs"].numpy()
+        for n in range(wl.n_branches):
+            x = np.sort(p[wl.label_off[n]:wl.label_off[n + 1]])[::-1]
+            if x[0] - x[1] > 1e-4:
+                assert g.argmax[n].item() == want_am[n].item()
