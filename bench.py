@@ -412,7 +412,7 @@ def run_libsp(args, ws, rank, local):
         if ws > 1:
             torch.distributed.barrier()
         e0.record(stream)
-        clf._copy_stream.wait_event(e0)  # the timed steps' copies start after e0
+        clf.copy_stream.wait_event(e0)  # the timed steps' copies start after e0
         for _ in range(args.e2e_steps):
             e2e_step()
         e1.record(stream)

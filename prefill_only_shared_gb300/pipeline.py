@@ -17,6 +17,16 @@ import torch
 from . import sp
 
 
+def _torch_stream(stream, device):
+    """A torch stream object for `stream` (None: torch's current stream on
+    `device`; a raw cudaStream_t handle is wrapped)."""
+    if stream is None:
+        return torch.cuda.current_stream(device)
+    if isinstance(stream, torch.cuda.Stream):
+        return stream
+    return torch.cuda.ExternalStream(int(stream), device=device)
+
+
 @dataclass
 class PassOutputs:
     out: torch.Tensor  # bf16 [node_tokens, Hq, d] (device)
@@ -307,12 +317,8 @@ class SharedPrefixClassifier:
         into probs_out / argmax_out (pinned host tensors).  Asynchronous:
         synchronise `stream` before reading the outputs.  W stays on the
         device (model state)."""
-        st = self._torch_stream(stream)
-        if getattr(self, "_copy_stream", None) is None:
-            self._copy_stream = torch.cuda.Stream(self.device)
-            self._in_sets = [{}, {}]
-            self._in_free = [None, None]
-            self._in_next = 0
+        st = _torch_stream(stream, self.device)
+        cs = self.copy_stream
         i = self._in_next
         self._in_next ^= 1
         dev_in = self._in_sets[i]
@@ -320,9 +326,10 @@ class SharedPrefixClassifier:
         for name, src in srcs.items():
             d = dev_in.get(name)
             if d is None or d.numel() < src.numel() or d.dtype != src.dtype:
+                if self._in_free[i] is not None:
+                    self._in_free[i].synchronize()  # the old buffer's last reader is done
                 d = torch.empty(max(src.numel(), 1), dtype=src.dtype, device=self.device)
                 dev_in[name] = d
-        cs = self._copy_stream
         if self._in_free[i] is not None:
             cs.wait_event(self._in_free[i])  # the pass that read this set is done
         views = {}
@@ -350,12 +357,15 @@ class SharedPrefixClassifier:
         self._in_free[i] = done
         return res
 
-    def _torch_stream(self, stream):
-        if stream is None:
-            return torch.cuda.current_stream(self.device)
-        if isinstance(stream, torch.cuda.Stream):
-            return stream
-        return torch.cuda.ExternalStream(int(stream), device=self.device)
+    @property
+    def copy_stream(self) -> torch.cuda.Stream:
+        """The side stream run_from_host copies inputs on (created on first use)."""
+        if getattr(self, "_copy_stream", None) is None:
+            self._copy_stream = torch.cuda.Stream(self.device)
+            self._in_sets = [{}, {}]
+            self._in_free = [None, None]
+            self._in_next = 0
+        return self._copy_stream
 
     @property
     def last_launches(self) -> int:
@@ -446,7 +456,7 @@ class ContinuousBatcher:
         if (self._rows + nt > self.q.shape[0] or self._brs + nb > self.h.shape[0]
                 or self._labs + nl > self.label_ids.shape[0]):
             raise ValueError("ContinuousBatcher arenas are full: reset() or raise the capacities")
-        st = self._torch_stream(stream)
+        st = _torch_stream(stream, self.clf.device)
         with torch.cuda.stream(st):
             r0, b0, l0 = self._rows, self._brs, self._labs
             self.q[r0:r0 + nt].copy_(q, non_blocking=True)
@@ -459,17 +469,10 @@ class ContinuousBatcher:
         self._rows, self._brs, self._labs = r0 + nt, b0 + nb, l0 + nl
         return rid
 
-    def _torch_stream(self, stream):
-        if stream is None:
-            return torch.cuda.current_stream(self.clf.device)
-        if isinstance(stream, torch.cuda.Stream):
-            return stream
-        return torch.cuda.ExternalStream(int(stream), device=self.clf.device)
-
     def run(self, stream=None) -> int:
         """Form and enqueue every batch of the queue on `stream`; returns the
         number of batches.  Asynchronous: synchronise before reading results."""
-        st = self._torch_stream(stream)
+        st = _torch_stream(stream, self.clf.device)
         raw = st.cuda_stream
         clf = self.clf
         V = self.W.shape[0]
