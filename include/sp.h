@@ -527,6 +527,64 @@ sp_status sp_run_pass(const sp_shape* shape, int32_t n_branches, const int32_t* 
                       float* logprobs, float* lse_vocab, void* lm_ws, size_t lm_ws_bytes,
                       float* probs, int32_t* argmax, void* stream, sp_plan_stats* stats);
 
+/* One device input set of sp_run_pass_host, owned by the caller: device
+ * buffers the pass's inputs are copied into, a pinned host buffer the launch
+ * descriptor is staged in, and two CUDA events (cudaEvent_t, created by the
+ * caller; timing may be disabled).  done_event is recorded on `stream` at the
+ * end of every pass that used the set; copied_event on copy_stream once the
+ * set's copies are done.  A caller alternates two sets so that one pass's
+ * copies overlap the previous pass's kernels. */
+typedef struct sp_input_set {
+  void* q;               /* DEVICE bf16, q_rows rows of n_q_heads * head_dim   */
+  void* k;               /* DEVICE bf16, q_rows rows of n_kv_heads * head_dim  */
+  void* v;               /* DEVICE bf16, as k                                  */
+  void* h;               /* DEVICE bf16, h_rows rows of hidden                 */
+  int32_t* label_off;    /* DEVICE int32, h_rows + 1                           */
+  int32_t* label_ids;    /* DEVICE int32, labels_cap                           */
+  int64_t q_rows;
+  int64_t h_rows;
+  int64_t labels_cap;
+  void* desc_host;       /* pinned HOST, desc_host_bytes                       */
+  size_t desc_host_bytes;
+  void* done_event;      /* cudaEvent_t                                        */
+  void* copied_event;    /* cudaEvent_t                                        */
+} sp_input_set;
+
+/* sp_run_pass with its inputs and outputs in pinned host memory: the same
+ * pass, plus the copies a caller holding host buffers needs, enqueued
+ * without blocking on the pass's own work.
+ *   1. plans and checks every capacity (as sp_run_pass; the set's q_rows,
+ *      h_rows, labels_cap and desc_host_bytes too, SP_ERR_WORKSPACE) and the
+ *      host label CSR (sp_check_labels, SP_ERR_ARG), before anything is
+ *      enqueued;
+ *   2. waits on the host for set->done_event: the last pass that used the
+ *      set has finished, so its buffers and staging can be overwritten;
+ *   3. on copy_stream: copies q_host, k_host, v_host (node_rows rows each),
+ *      h_host (n_branches rows), label_off_host (n_branches + 1) and
+ *      label_ids_host (n_labels) into the set, then records copied_event;
+ *   4. on stream: waits for copied_event, uploads the descriptor from
+ *      desc_host, runs the tree attention, readout and softmax on the set's
+ *      buffers, copies probs and argmax to probs_host and argmax_host, and
+ *      records done_event.
+ * Once step 3 has been enqueued, done_event is recorded even when a later
+ * step fails.  The outputs in host memory are ready once done_event has
+ * completed (or `stream` is synchronised).  All host buffers but tokens and
+ * the CSRs must be pinned for the copies to run asynchronously; pageable
+ * ones still work but their copies block the host.  Other arguments and
+ * errors are as for sp_run_pass. */
+sp_status sp_run_pass_host(const sp_shape* shape, int32_t n_branches,
+                           const int32_t* req_of_branch, const int64_t* tok_offsets,
+                           const int32_t* tokens, int64_t node_rows, const void* q_host,
+                           const void* k_host, const void* v_host, const void* h_host,
+                           const int32_t* label_off_host, const int32_t* label_ids_host,
+                           int32_t n_labels, const sp_input_set* set, void* kv_pool,
+                           int32_t pool_pages, void* out, float* lse, void* desc,
+                           size_t desc_bytes, void* attn_ws, size_t attn_ws_bytes, const void* W,
+                           float* logprobs, float* lse_vocab, void* lm_ws, size_t lm_ws_bytes,
+                           float* probs, int32_t* argmax, float* probs_host,
+                           int32_t* argmax_host, void* stream, void* copy_stream,
+                           sp_plan_stats* stats);
+
 /* Host-side validation of the option CSRs of sp_option_softmax (HOST
  * arrays): opt_off starts at 0, increases strictly and ends <= n_rows; q_off
  * starts at 0, ends <= n_opts, and gives every question 2..64 options.

@@ -362,6 +362,62 @@ extern "C" sp_status sp_option_softmax(const float* row_logprobs, int32_t n_rows
   return e == cudaSuccess ? SP_OK : SP_ERR_CUDA;
 }
 
+namespace {
+
+// Plans a whole pass (without a page limit, so that a pool that is too small
+// still reports the pages needed) and checks every capacity of sp_run_pass.
+// On SP_OK *plan is the caller's to free; otherwise it is freed here.
+sp_status plan_pass(const sp_shape* shape, int32_t n_branches, const int32_t* req_of_branch,
+                    const int64_t* tok_offsets, const int32_t* tokens, int64_t node_rows,
+                    int32_t pool_pages, size_t desc_bytes, size_t attn_ws_bytes,
+                    size_t lm_ws_bytes, sp_plan** plan, sp_plan_stats* stats) {
+  sp_status st = sp_plan_build(shape, n_branches, req_of_branch, tok_offsets, tokens, INT32_MAX,
+                               sm_count(), plan);
+  if (st != SP_OK) return st;
+  sp_plan_stats ps;
+  sp_plan_get_stats(*plan, &ps);
+  if (stats) *stats = ps;
+  const size_t lm_need = sp::lmhead_workspace_bytes(n_branches, shape->vocab, sm_count());
+  if (ps.node_tokens != node_rows) st = SP_ERR_ARG;
+  else if (ps.pages_used > pool_pages) st = SP_ERR_POOL_FULL;
+  else if ((size_t)ps.desc_bytes > desc_bytes || (size_t)ps.attn_workspace_bytes > attn_ws_bytes ||
+           lm_ws_bytes < lm_need)
+    st = SP_ERR_WORKSPACE;
+  if (st != SP_OK) {
+    sp_plan_free(*plan);
+    *plan = nullptr;
+  }
+  return st;
+}
+
+// The launches of a pass whose descriptor is already enqueued for upload:
+// one tree attention call, the readout and the label softmax.
+sp_status launch_pass(const sp_plan* plan, const sp_shape* shape, int32_t n_branches,
+                      const void* desc, const void* q, const void* k, const void* v,
+                      void* kv_pool, void* out, float* lse, void* attn_ws, size_t attn_ws_bytes,
+                      const void* h, const void* W, const int32_t* label_off,
+                      const int32_t* label_ids, int32_t n_labels, float* logprobs,
+                      float* lse_vocab, void* lm_ws, size_t lm_ws_bytes, float* probs,
+                      int32_t* argmax, void* stream) {
+  int32_t launches = 0;
+  sp_status st = sp_tree_attn(plan, desc, SP_ALL_ROUNDS, q, k, v, kv_pool, out, lse, attn_ws,
+                              attn_ws_bytes, stream);
+  launches += t_last_launches;
+  if (st == SP_OK) {
+    st = sp_label_logprobs(h, W, n_branches, shape->hidden, shape->vocab, label_off, label_ids,
+                           n_labels, logprobs, lse_vocab, lm_ws, lm_ws_bytes, stream);
+    launches += t_last_launches;
+  }
+  if (st == SP_OK) {
+    st = sp_label_softmax(logprobs, label_off, n_branches, probs, argmax, stream);
+    launches += t_last_launches;
+  }
+  t_last_launches = launches;
+  return st;
+}
+
+}  // namespace
+
 extern "C" sp_status sp_run_pass(const sp_shape* shape, int32_t n_branches,
                                    const int32_t* req_of_branch, const int64_t* tok_offsets,
                                    const int32_t* tokens, int64_t node_rows, const void* q,
@@ -376,42 +432,96 @@ extern "C" sp_status sp_run_pass(const sp_shape* shape, int32_t n_branches,
   t_last_launches = 0;
   if (!shape || !probs || !argmax) return SP_ERR_ARG;
   sp_plan* plan = nullptr;
-  // planned without a page limit, so that a pool that is too small still
-  // reports the pages needed
-  sp_status st = sp_plan_build(shape, n_branches, req_of_branch, tok_offsets, tokens, INT32_MAX,
-                               sm_count(), &plan);
+  sp_status st = plan_pass(shape, n_branches, req_of_branch, tok_offsets, tokens, node_rows,
+                           pool_pages, desc_bytes, attn_ws_bytes, lm_ws_bytes, &plan, stats);
   if (st != SP_OK) return st;
-  sp_plan_stats ps;
-  sp_plan_get_stats(plan, &ps);
-  if (stats) *stats = ps;
-  // every capacity is checked before the first launch
-  const size_t lm_need =
-      sp::lmhead_workspace_bytes(n_branches, shape->vocab, sm_count());
-  if (ps.node_tokens != node_rows) st = SP_ERR_ARG;
-  else if (ps.pages_used > pool_pages) st = SP_ERR_POOL_FULL;
-  else if ((size_t)ps.desc_bytes > desc_bytes || (size_t)ps.attn_workspace_bytes > attn_ws_bytes ||
-           lm_ws_bytes < lm_need)
-    st = SP_ERR_WORKSPACE;
-  int32_t launches = 0;
-  if (st == SP_OK) st = sp_plan_upload(plan, desc, desc_bytes, stream);
-  if (st == SP_OK) {
-    st = sp_tree_attn(plan, desc, SP_ALL_ROUNDS, q, k, v, kv_pool, out, lse, attn_ws,
-                      attn_ws_bytes, stream);
-    launches += t_last_launches;
-  }
+  st = sp_plan_upload(plan, desc, desc_bytes, stream);
+  if (st == SP_OK)
+    st = launch_pass(plan, shape, n_branches, desc, q, k, v, kv_pool, out, lse, attn_ws,
+                     attn_ws_bytes, h, W, label_off, label_ids, n_labels, logprobs, lse_vocab,
+                     lm_ws, lm_ws_bytes, probs, argmax, stream);
   // the upload staged the descriptor out of the plan's (pageable) memory
   // before returning, so the plan can go
   sp_plan_free(plan);
-  if (st == SP_OK) {
-    st = sp_label_logprobs(h, W, n_branches, shape->hidden, shape->vocab, label_off, label_ids,
-                           n_labels, logprobs, lse_vocab, lm_ws, lm_ws_bytes, stream);
-    launches += t_last_launches;
+  return st;
+}
+
+extern "C" sp_status sp_run_pass_host(
+    const sp_shape* shape, int32_t n_branches, const int32_t* req_of_branch,
+    const int64_t* tok_offsets, const int32_t* tokens, int64_t node_rows, const void* q_host,
+    const void* k_host, const void* v_host, const void* h_host, const int32_t* label_off_host,
+    const int32_t* label_ids_host, int32_t n_labels, const sp_input_set* set, void* kv_pool,
+    int32_t pool_pages, void* out, float* lse, void* desc, size_t desc_bytes, void* attn_ws,
+    size_t attn_ws_bytes, const void* W, float* logprobs, float* lse_vocab, void* lm_ws,
+    size_t lm_ws_bytes, float* probs, int32_t* argmax, float* probs_host, int32_t* argmax_host,
+    void* stream, void* copy_stream, sp_plan_stats* stats) {
+  t_last_launches = 0;
+  if (!shape || !set || !q_host || !k_host || !v_host || !h_host || !label_off_host ||
+      !label_ids_host || !probs || !argmax || !probs_host || !argmax_host || !set->q || !set->k ||
+      !set->v || !set->h || !set->label_off || !set->label_ids || !set->desc_host ||
+      !set->done_event || !set->copied_event || !desc || n_branches < 1 || n_labels < 1)
+    return SP_ERR_ARG;
+  if (label_off_host[0] != 0 || label_off_host[n_branches] != n_labels) return SP_ERR_ARG;
+  sp_status st = sp_check_labels(label_off_host, label_ids_host, n_branches, shape->vocab);
+  if (st != SP_OK) return st;
+  sp_plan* plan = nullptr;
+  st = plan_pass(shape, n_branches, req_of_branch, tok_offsets, tokens, node_rows, pool_pages,
+                 desc_bytes, attn_ws_bytes, lm_ws_bytes, &plan, stats);
+  if (st != SP_OK) return st;
+  const size_t blob = plan->blob.size();
+  if (node_rows > set->q_rows || n_branches > set->h_rows || n_labels > set->labels_cap ||
+      blob > set->desc_host_bytes) {
+    sp_plan_free(plan);
+    return SP_ERR_WORKSPACE;
   }
-  if (st == SP_OK) {
-    st = sp_label_softmax(logprobs, label_off, n_branches, probs, argmax, stream);
-    launches += t_last_launches;
+  if (reinterpret_cast<uintptr_t>(desc) & 255u) {
+    sp_plan_free(plan);
+    return SP_ERR_ARG;
   }
-  t_last_launches = launches;
+  const auto done = static_cast<cudaEvent_t>(set->done_event);
+  const auto copied = static_cast<cudaEvent_t>(set->copied_event);
+  const auto cs = static_cast<cudaStream_t>(copy_stream);
+  const auto ms = static_cast<cudaStream_t>(stream);
+  // the last pass that used this set has read its inputs and its staged
+  // descriptor (an event that was never recorded counts as done)
+  if (cudaEventSynchronize(done) != cudaSuccess) {
+    sp_plan_free(plan);
+    return SP_ERR_CUDA;
+  }
+  std::memcpy(set->desc_host, plan->blob.data(), blob);
+  const size_t e = 2;  // bf16
+  const size_t q_bytes = (size_t)node_rows * shape->n_q_heads * shape->head_dim * e;
+  const size_t kv_bytes = (size_t)node_rows * shape->n_kv_heads * shape->head_dim * e;
+  const size_t h_bytes = (size_t)n_branches * shape->hidden * e;
+  cudaError_t ce = cudaSuccess;
+  const void* src[6] = {q_host, k_host, v_host, h_host, label_off_host, label_ids_host};
+  void* dst[6] = {set->q, set->k, set->v, set->h, set->label_off, set->label_ids};
+  const size_t bytes[6] = {q_bytes, kv_bytes, kv_bytes, h_bytes,
+                           ((size_t)n_branches + 1) * sizeof(int32_t),
+                           (size_t)n_labels * sizeof(int32_t)};
+  for (int i = 0; i < 6 && ce == cudaSuccess; ++i)
+    ce = cudaMemcpyAsync(dst[i], src[i], bytes[i], cudaMemcpyHostToDevice, cs);
+  // however many copies were enqueued, they finish before anything `stream`
+  // runs from here on, done_event included
+  cudaError_t cw = cudaEventRecord(copied, cs);
+  if (cw == cudaSuccess) cw = cudaStreamWaitEvent(ms, copied, 0);
+  if (cw != cudaSuccess) cudaStreamSynchronize(cs);
+  st = ce == cudaSuccess && cw == cudaSuccess ? SP_OK : SP_ERR_CUDA;
+  if (st == SP_OK &&
+      cudaMemcpyAsync(desc, set->desc_host, blob, cudaMemcpyHostToDevice, ms) != cudaSuccess)
+    st = SP_ERR_CUDA;
+  if (st == SP_OK)
+    st = launch_pass(plan, shape, n_branches, desc, set->q, set->k, set->v, kv_pool, out, lse,
+                     attn_ws, attn_ws_bytes, set->h, W, set->label_off, set->label_ids, n_labels,
+                     logprobs, lse_vocab, lm_ws, lm_ws_bytes, probs, argmax, stream);
+  sp_plan_free(plan);
+  if (st == SP_OK &&
+      (cudaMemcpyAsync(probs_host, probs, (size_t)n_labels * sizeof(float),
+                       cudaMemcpyDeviceToHost, ms) != cudaSuccess ||
+       cudaMemcpyAsync(argmax_host, argmax, (size_t)n_branches * sizeof(int32_t),
+                       cudaMemcpyDeviceToHost, ms) != cudaSuccess))
+    st = SP_ERR_CUDA;
+  if (cudaEventRecord(done, ms) != cudaSuccess && st == SP_OK) st = SP_ERR_CUDA;
   return st;
 }
 

@@ -259,18 +259,10 @@ class SharedPrefixClassifier:
             h, W, label_off, label_ids, n_labels, stream, qtype)
         return PassOutputs(out, lse, logprobs, lse_v, probs, argmax, plan, value, conf)
 
-    def run_pass(self, req_of_branch, tok_offsets, tokens, q, k, v, h, W, label_off, label_ids,
-                 stream=None) -> PassOutputs:
-        """The whole pass in one native call (sp_run_pass: plan, upload, one
-        tree attention call, readout, softmax), so the host work is the C++
-        planner's.  Buffers grow when the call reports SP_ERR_WORKSPACE or
-        SP_ERR_POOL_FULL (nothing is launched then) and the call is repeated.
-        Not with a prefix cache (its plans come from sp_plan_build_cached)."""
-        if self.cache is not None:
-            raise ValueError("run_pass plans without the prefix cache")
-        stream = self._stream(stream)
+    def _pass_outputs(self, T, N, nl, W):
+        """Output and readout buffers of a whole pass: T node rows, N branches,
+        nl labels."""
         s = self.shape
-        T, N, nl = int(q.shape[0]), int(h.shape[0]), int(label_ids.numel())
         out = self._buf("out", T * s.n_q_heads * s.head_dim, torch.bfloat16).view(
             T, s.n_q_heads, s.head_dim)
         lse = self._buf("lse", T * s.n_q_heads, torch.float32).view(T, s.n_q_heads)
@@ -285,6 +277,31 @@ class SharedPrefixClassifier:
         lm_ws = self._buf("lm_ws", self._lm_ws_bytes, torch.uint8)
         if not hasattr(self, "_pass_need"):
             self._pass_need = {"desc_bytes": 4096, "attn_workspace_bytes": 0}
+        return out, lse, logprobs, lse_v, probs, argmax, lm_ws
+
+    def _grow_pass_needs(self, status, st, where):
+        """After SP_ERR_WORKSPACE / SP_ERR_POOL_FULL from a whole-pass call:
+        grow the descriptor, workspace and pool sizes to what it reported."""
+        need = self._pass_need
+        need["desc_bytes"] = max(need["desc_bytes"], st["desc_bytes"])
+        need["attn_workspace_bytes"] = max(need["attn_workspace_bytes"], st["attn_workspace_bytes"])
+        if status == 3:  # SP_ERR_POOL_FULL
+            if self.fixed_pool:
+                raise sp.SpError(status, where)
+            self._ensure_pool(st["pages_used"])
+
+    def run_pass(self, req_of_branch, tok_offsets, tokens, q, k, v, h, W, label_off, label_ids,
+                 stream=None) -> PassOutputs:
+        """The whole pass in one native call (sp_run_pass: plan, upload, one
+        tree attention call, readout, softmax), so the host work is the C++
+        planner's.  Buffers grow when the call reports SP_ERR_WORKSPACE or
+        SP_ERR_POOL_FULL (nothing is launched then) and the call is repeated.
+        Not with a prefix cache (its plans come from sp_plan_build_cached)."""
+        if self.cache is not None:
+            raise ValueError("run_pass plans without the prefix cache")
+        stream = self._stream(stream)
+        out, lse, logprobs, lse_v, probs, argmax, lm_ws = self._pass_outputs(
+            int(q.shape[0]), int(h.shape[0]), int(label_ids.numel()), W)
         for _ in range(3):
             need = self._pass_need
             desc = self._desc_view(need["desc_bytes"])
@@ -294,13 +311,7 @@ class SharedPrefixClassifier:
                                         label_ids, logprobs, lse_v, lm_ws, probs, argmax, stream)
             if status == sp.SP_OK:
                 break
-            need["desc_bytes"] = max(need["desc_bytes"], st["desc_bytes"])
-            need["attn_workspace_bytes"] = max(need["attn_workspace_bytes"],
-                                               st["attn_workspace_bytes"])
-            if status == 3:  # SP_ERR_POOL_FULL
-                if self.fixed_pool:
-                    raise sp.SpError(status, "sp_run_pass")
-                self._ensure_pool(st["pages_used"])
+            self._grow_pass_needs(status, st, "sp_run_pass")
         else:
             raise sp.SpError(status, "sp_run_pass")
         self.last_pass_launches = sp.sp_last_launch_count()
@@ -316,55 +327,119 @@ class SharedPrefixClassifier:
         its copies are done, and its probabilities and argmax are copied out
         into probs_out / argmax_out (pinned host tensors).  Asynchronous:
         synchronise `stream` before reading the outputs.  W stays on the
-        device (model state)."""
+        device (model state).  The tree schedule without question types or a
+        prefix cache is one native call (sp_run_pass_host: copies, pass and
+        read-back); the other forms copy through torch and call ``run``."""
         st = _torch_stream(stream, self.device)
         cs = self.copy_stream
         i = self._in_next
         self._in_next ^= 1
-        dev_in = self._in_sets[i]
         srcs = {"q": q, "k": k, "v": v, "h": h, "label_off": label_off, "label_ids": label_ids}
-        for name, src in srcs.items():
-            d = dev_in.get(name)
-            if d is None or d.numel() < src.numel() or d.dtype != src.dtype:
-                if self._in_free[i] is not None:
-                    self._in_free[i].synchronize()  # the old buffer's last reader is done
-                d = torch.empty(max(src.numel(), 1), dtype=src.dtype, device=self.device)
-                dev_in[name] = d
-        if self._in_free[i] is not None:
-            cs.wait_event(self._in_free[i])  # the pass that read this set is done
+        self._grow_input_set(i, srcs)
+        if schedule == "tree" and qtype is None and self.cache is None:
+            return self._run_pass_host(i, req_of_branch, tok_offsets, tokens, srcs, W, probs_out,
+                                       argmax_out, st, cs)
+        dev_in = self._in_sets[i]
+        cs.wait_event(self._in_done[i])  # the pass that read this set is done
         views = {}
         with torch.cuda.stream(cs):
             for name, src in srcs.items():
                 view = dev_in[name][:src.numel()].view(src.shape)
                 view.copy_(src, non_blocking=True)
                 views[name] = view
-            copied = torch.cuda.Event()
-            copied.record(cs)
-        st.wait_event(copied)
-        if schedule == "tree" and qtype is None and self.cache is None:
-            res = self.run_pass(req_of_branch, tok_offsets, tokens, views["q"], views["k"],
-                                views["v"], views["h"], W, views["label_off"],
-                                views["label_ids"], st.cuda_stream)
-        else:
-            res = self.run(req_of_branch, tok_offsets, tokens, views["q"], views["k"], views["v"],
-                           views["h"], W, views["label_off"], views["label_ids"], st.cuda_stream,
-                           schedule, qtype)
+            self._in_copied[i].record(cs)
+        st.wait_event(self._in_copied[i])
+        res = self.run(req_of_branch, tok_offsets, tokens, views["q"], views["k"], views["v"],
+                       views["h"], W, views["label_off"], views["label_ids"], st.cuda_stream,
+                       schedule, qtype)
         with torch.cuda.stream(st):
             probs_out.copy_(res.probs, non_blocking=True)
             argmax_out.copy_(res.argmax, non_blocking=True)
-            done = torch.cuda.Event()
-            done.record(st)
-        self._in_free[i] = done
+            self._in_done[i].record(st)
         return res
+
+    def _grow_input_set(self, i, srcs):
+        """Grow device input set i to hold `srcs`; a buffer is replaced only
+        after the last pass that read the set has finished."""
+        dev_in = self._in_sets[i]
+        for name, src in srcs.items():
+            d = dev_in.get(name)
+            if d is None or d.numel() < src.numel() or d.dtype != src.dtype:
+                self._in_done[i].synchronize()
+                dev_in[name] = torch.empty(max(src.numel(), 1), dtype=src.dtype,
+                                           device=self.device)
+                self._in_struct[i] = None
+
+    def _input_struct(self, i, desc_bytes):
+        """The sp_input_set of device input set i, with at least desc_bytes of
+        pinned descriptor staging."""
+        c = self._in_struct[i]
+        if c is not None and c.desc_host_bytes >= desc_bytes:
+            return c
+        dh = self._in_desc_host[i]
+        if dh is None or dh.numel() < desc_bytes:
+            self._in_done[i].synchronize()  # its last upload has run
+            dh = torch.empty(int(desc_bytes), dtype=torch.uint8).pin_memory()
+            self._in_desc_host[i] = dh
+        d, s = self._in_sets[i], self.shape
+        rows = min(d["q"].numel() // (s.n_q_heads * s.head_dim),
+                   d["k"].numel() // (s.n_kv_heads * s.head_dim),
+                   d["v"].numel() // (s.n_kv_heads * s.head_dim))
+        c = sp.sp_input_set(
+            q=d["q"].data_ptr(), k=d["k"].data_ptr(), v=d["v"].data_ptr(), h=d["h"].data_ptr(),
+            label_off=d["label_off"].data_ptr(), label_ids=d["label_ids"].data_ptr(),
+            q_rows=rows, h_rows=min(d["h"].numel() // s.hidden, d["label_off"].numel() - 1),
+            labels_cap=d["label_ids"].numel(), desc_host=dh.data_ptr(),
+            desc_host_bytes=dh.numel(), done_event=self._in_done[i].cuda_event,
+            copied_event=self._in_copied[i].cuda_event)
+        self._in_struct[i] = c
+        return c
+
+    def _run_pass_host(self, i, req_of_branch, tok_offsets, tokens, srcs, W, probs_out,
+                       argmax_out, st, cs) -> PassOutputs:
+        s = self.shape
+        q, k, v, h = srcs["q"], srcs["k"], srcs["v"], srcs["h"]
+        T, N = int(q.shape[0]), int(h.shape[0])
+        if (q.numel() != T * s.n_q_heads * s.head_dim or k.numel() != T * s.n_kv_heads * s.head_dim
+                or v.numel() != k.numel() or h.numel() != N * s.hidden
+                or srcs["label_off"].numel() != N + 1 or probs_out.numel() < srcs["label_ids"].numel()
+                or argmax_out.numel() < N):
+            raise ValueError("host inputs / outputs do not match the model shape")
+        out, lse, logprobs, lse_v, probs, argmax, lm_ws = self._pass_outputs(
+            T, N, int(srcs["label_ids"].numel()), W)
+        for _ in range(3):
+            need = self._pass_need
+            desc = self._desc_view(need["desc_bytes"])
+            ws = self._buf("attn_ws", need["attn_workspace_bytes"], torch.uint8)
+            iset = self._input_struct(i, need["desc_bytes"])
+            status, stt = sp.sp_run_pass_host(
+                s, req_of_branch, tok_offsets, tokens, q, k, v, h, srcs["label_off"],
+                srcs["label_ids"], iset, self.kv_pool, out, lse, desc, ws, W, logprobs, lse_v,
+                lm_ws, probs, argmax, probs_out, argmax_out, st.cuda_stream, cs.cuda_stream)
+            if status == sp.SP_OK:
+                break
+            self._grow_pass_needs(status, stt, "sp_run_pass_host")
+        else:
+            raise sp.SpError(status, "sp_run_pass_host")
+        self.last_pass_launches = sp.sp_last_launch_count()
+        return PassOutputs(out, lse, logprobs, lse_v, probs, argmax, None)
 
     @property
     def copy_stream(self) -> torch.cuda.Stream:
         """The side stream run_from_host copies inputs on (created on first use)."""
         if getattr(self, "_copy_stream", None) is None:
-            self._copy_stream = torch.cuda.Stream(self.device)
+            cs = torch.cuda.Stream(self.device)
             self._in_sets = [{}, {}]
-            self._in_free = [None, None]
+            self._in_struct = [None, None]
+            self._in_desc_host = [None, None]
             self._in_next = 0
+            # per set: done (its last pass has finished) and copied (its
+            # inputs are in); recorded once here so that each has a CUDA event
+            self._in_done = [torch.cuda.Event(), torch.cuda.Event()]
+            self._in_copied = [torch.cuda.Event(), torch.cuda.Event()]
+            for e in self._in_done + self._in_copied:
+                e.record(cs)
+            self._copy_stream = cs
         return self._copy_stream
 
     @property

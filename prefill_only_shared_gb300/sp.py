@@ -54,6 +54,15 @@ _I32P = ctypes.POINTER(ctypes.c_int32)
 _I64P = ctypes.POINTER(ctypes.c_int64)
 _SZ = ctypes.c_size_t
 
+
+class sp_input_set(ctypes.Structure):
+    """One device input set of sp_run_pass_host (device buffers, pinned
+    descriptor staging, the set's two CUDA events)."""
+    _fields_ = [("q", _P), ("k", _P), ("v", _P), ("h", _P), ("label_off", _P),
+                ("label_ids", _P), ("q_rows", ctypes.c_int64), ("h_rows", ctypes.c_int64),
+                ("labels_cap", ctypes.c_int64), ("desc_host", _P), ("desc_host_bytes", _SZ),
+                ("done_event", _P), ("copied_event", _P)]
+
 # Every symbol declared in include/sp.h, with its ctypes signature.
 SIGNATURES = {
     "sp_plan_build": (_I32, [ctypes.POINTER(sp_shape), _I32, _I32P, _I64P, _I32P, _I32, _I32,
@@ -96,6 +105,11 @@ SIGNATURES = {
     "sp_run_pass": (_I32, [ctypes.POINTER(sp_shape), _I32, _I32P, _I64P, _I32P, ctypes.c_int64,
                            _P, _P, _P, _P, _I32, _P, _P, _P, _SZ, _P, _SZ, _P, _P, _P, _P, _I32,
                            _P, _P, _P, _SZ, _P, _P, _P, ctypes.POINTER(sp_plan_stats)]),
+    "sp_run_pass_host": (_I32, [ctypes.POINTER(sp_shape), _I32, _I32P, _I64P, _I32P,
+                                ctypes.c_int64, _P, _P, _P, _P, _P, _P, _I32,
+                                ctypes.POINTER(sp_input_set), _P, _I32, _P, _P, _P, _SZ, _P, _SZ,
+                                _P, _P, _P, _P, _SZ, _P, _P, _P, _P, _P, _P,
+                                ctypes.POINTER(sp_plan_stats)]),
     "sp_check_options": (_I32, [_I32P, _I32, _I32, _I32P, _I32]),
     "sp_check_device_error": (_I32, [_P]),
     "sp_status_str": (ctypes.c_char_p, [_I32]),
@@ -514,6 +528,50 @@ def sp_run_pass(shape: sp_shape, req_of_branch, tok_offsets, tokens, q, k, v, kv
         _stream(stream), ctypes.byref(st))
     if status not in (SP_OK, 3, 7):  # SP_ERR_POOL_FULL, SP_ERR_WORKSPACE: the caller grows
         _check(status, "sp_run_pass")
+    return status, st.as_dict()
+
+
+def _host(t: torch.Tensor, dtype, name: str):
+    if not isinstance(t, torch.Tensor) or t.device.type != "cpu":
+        raise ValueError(f"{name} must be a host tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def sp_run_pass_host(shape: sp_shape, req_of_branch, tok_offsets, tokens, q_host, k_host, v_host,
+                     h_host, label_off_host, label_ids_host, in_set: sp_input_set, kv_pool, out,
+                     lse, desc, attn_ws, W, logprobs, lse_vocab, lm_ws, probs, argmax, probs_host,
+                     argmax_host, stream, copy_stream):
+    """sp_run_pass with host inputs and outputs (pinned for asynchronous
+    copies), copied through the device input set `in_set`.  Returns (status,
+    plan stats dict) as sp_run_pass: SP_ERR_WORKSPACE and SP_ERR_POOL_FULL come
+    back with the stats (nothing enqueued); other errors raise."""
+    req = _np(req_of_branch, np.int32)
+    off = _np(tok_offsets, np.int64)
+    tok = _np(tokens, np.int32)
+    st = sp_plan_stats()
+    status = lib().sp_run_pass_host(
+        ctypes.byref(shape), len(req), req.ctypes.data_as(_I32P), off.ctypes.data_as(_I64P),
+        tok.ctypes.data_as(_I32P), int(q_host.shape[0]),
+        _host(q_host, torch.bfloat16, "q_host"), _host(k_host, torch.bfloat16, "k_host"),
+        _host(v_host, torch.bfloat16, "v_host"), _host(h_host, torch.bfloat16, "h_host"),
+        _host(label_off_host, torch.int32, "label_off_host"),
+        _host(label_ids_host, torch.int32, "label_ids_host"), label_ids_host.numel(),
+        ctypes.byref(in_set), _dev(kv_pool, torch.bfloat16, "kv_pool"), int(kv_pool.shape[0]),
+        _dev(out, torch.bfloat16, "out"), _dev(lse, torch.float32, "lse"),
+        _dev(desc, torch.uint8, "desc"), desc.numel(),
+        _dev(attn_ws, torch.uint8, "attn_ws") if attn_ws.numel() else None, attn_ws.numel(),
+        _dev(W, torch.bfloat16, "W"), _dev(logprobs, torch.float32, "logprobs"),
+        _dev(lse_vocab, torch.float32, "lse_vocab"), _dev(lm_ws, torch.uint8, "lm_ws"),
+        lm_ws.numel(), _dev(probs, torch.float32, "probs"), _dev(argmax, torch.int32, "argmax"),
+        _host(probs_host, torch.float32, "probs_host"),
+        _host(argmax_host, torch.int32, "argmax_host"), _stream(stream), _stream(copy_stream),
+        ctypes.byref(st))
+    if status not in (SP_OK, 3, 7):  # SP_ERR_POOL_FULL, SP_ERR_WORKSPACE: the caller grows
+        _check(status, "sp_run_pass_host")
     return status, st.as_dict()
 
 

@@ -169,3 +169,78 @@ def test_check_options(lib):
                                    ([0] + list(range(1, 67)), 66, [0, 66])):  # 66 options
         with pytest.raises(lib.SpError):
             lib.sp_check_options(opt_off, n_rows, q_off)
+
+
+def test_struct_layouts_match_the_header(lib, tmp_path):
+    """The ctypes structures of the binding have the C compiler's size and
+    field offsets for every struct the header declares by value."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    structs = {"sp_shape": lib.sp_shape, "sp_plan_stats": lib.sp_plan_stats,
+               "sp_input_set": lib.sp_input_set}
+    lines = ["#include <stdio.h>", "#include <stddef.h>", f'#include "{HEADER}"',
+             "int main(void) {"]
+    for name, cls in structs.items():
+        lines.append(f'  printf("{name} %zu\\n", sizeof({name}));')
+        for f, _ in cls._fields_:
+            lines.append(f'  printf("{name}.{f} %zu\\n", offsetof({name}, {f}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c99", "-o", str(exe), str(src)], check=True)
+    got = dict(l.split() for l in subprocess.run([str(exe)], check=True, capture_output=True,
+                                                  text=True).stdout.splitlines())
+    for name, cls in structs.items():
+        assert int(got[name]) == ctypes.sizeof(cls), name
+        for f, _ in cls._fields_:
+            assert int(got[f"{name}.{f}"]) == getattr(cls, f).offset, (name, f)
+
+
+def test_host_pass_checks_before_any_copy(lib):
+    """sp_run_pass_host validates the host label CSR and every capacity (the
+    input set's included) before it enqueues anything: these calls return
+    before any CUDA call, so the device pointers are placeholders that are
+    never dereferenced."""
+    sh = lib.make_shape(8, 2, 64, 16, 64, 100)
+    off, toks = csr([[1, 2, 3, 4], [1, 2, 3, 5]])
+    req = np.zeros(2, np.int32)
+    T = 5  # node rows: 3 shared + 1 + 1
+    q = np.zeros(T * 8 * 64, np.uint16)
+    k = np.zeros(T * 2 * 64, np.uint16)
+    h = np.zeros(2 * 64, np.uint16)
+    lab_off = np.array([0, 2, 4], np.int32)
+    lab_ids = np.array([1, 2, 3, 4], np.int32)
+    probs_h = np.zeros(4, np.float32)
+    am_h = np.zeros(2, np.int32)
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced on these paths
+
+    def call(lab_off, lab_ids, q_rows, desc_host_bytes=1 << 20):
+        iset = lib.sp_input_set(q=fake, k=fake, v=fake, h=fake, label_off=fake, label_ids=fake,
+                                q_rows=q_rows, h_rows=2, labels_cap=4, desc_host=fake,
+                                desc_host_bytes=desc_host_bytes, done_event=fake,
+                                copied_event=fake)
+        st = lib.sp_plan_stats()
+        P = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+        status = lib.lib().sp_run_pass_host(
+            ctypes.byref(sh), 2, req.ctypes.data_as(lib._I32P), off.ctypes.data_as(lib._I64P),
+            toks.ctypes.data_as(lib._I32P), T, P(q), P(k), P(k), P(h),
+            lab_off.ctypes.data_as(ctypes.c_void_p), lab_ids.ctypes.data_as(ctypes.c_void_p),
+            len(lab_ids), ctypes.byref(iset), fake, 1 << 20, fake, fake, fake, 1 << 20, fake,
+            1 << 24, fake, fake, fake, fake, 1 << 26, fake, fake, P(probs_h), P(am_h), None, None,
+            ctypes.byref(st))
+        return status, st.as_dict()
+
+    # a label count of 1, an id past the vocabulary, offsets that do not end at n_labels
+    for lo, li in (([0, 1, 4], [1, 2, 3, 4]), ([0, 2, 4], [1, 2, 3, 100]),
+                   ([0, 2, 3], [1, 2, 3, 4])):
+        assert call(np.array(lo, np.int32), np.array(li, np.int32), T)[0] == 1
+    # the input set holds fewer node rows than the pass: SP_ERR_WORKSPACE, stats filled
+    status, st = call(lab_off, lab_ids, T - 1)
+    assert status == 7 and st["node_tokens"] == T and st["n_branches"] == 2
+    # descriptor staging shorter than the plan's descriptor
+    status, st = call(lab_off, lab_ids, T, desc_host_bytes=st["desc_bytes"] - 1)
+    assert status == 7
