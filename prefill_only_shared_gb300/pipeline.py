@@ -74,6 +74,10 @@ class SharedPrefixClassifier:
         if self.kv_pool is not None and self.kv_pool.shape[0] >= pages:
             return
         s = self.shape
+        if self.kv_pool is not None:
+            # passes enqueued on other streams may still read the old pool:
+            # let them finish before its memory can be handed out again
+            torch.cuda.synchronize(self.device)
         self.kv_pool = torch.empty((max(pages, 1), 2, s.n_kv_heads, s.page_size, s.head_dim),
                                    dtype=torch.bfloat16, device=self.device)
 
@@ -90,6 +94,8 @@ class SharedPrefixClassifier:
             return view
         b = self._bufs.get(name)
         if b is None or b.numel() < numel or b.dtype != dtype:
+            if b is not None:  # as for the pool: the old buffer's readers finish first
+                torch.cuda.synchronize(self.device)
             b = torch.empty(max(int(numel), 1), dtype=dtype, device=self.device)
             self._bufs[name] = b
             self._views = {k: v for k, v in self._views.items() if k[0] != name}
