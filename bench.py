@@ -512,6 +512,15 @@ def run_libsp(args, ws, rank, local):
         },
         "decisions_per_s": round(N * ws / (ms / 1e3), 1),
         "logical_tokens_per_s": round(stats["logical_tokens"] * ws / (ms / 1e3), 1),
+        # the same counts over the phases that compute them: branch tokens
+        # and logical tokens over the attention time, decisions over the
+        # readout and softmax time (the step-based figures above include
+        # every phase)
+        "per_phase": {
+            "branch_tokens_per_s_attention": round(branch_tokens * ws / (attn_avg / 1e3), 1),
+            "logical_tokens_per_s_attention": round(stats["logical_tokens"] * ws / (attn_avg / 1e3), 1),
+            "decisions_per_s_readout": round(N * ws / ((lm_avg + statistics.mean(sm_ms)) / 1e3), 1),
+        },
         "phase_ms": {"attention": round(attn_avg, 5), "label_logprobs": round(lm_avg, 5),
                      "label_softmax": round(statistics.mean(sm_ms), 5),
                      "plan_and_launch_overhead": round(ms - attn_avg - lm_avg - statistics.mean(sm_ms), 5)},
