@@ -244,3 +244,32 @@ def test_host_pass_checks_before_any_copy(lib):
     # descriptor staging shorter than the plan's descriptor
     status, st = call(lab_off, lab_ids, T, desc_host_bytes=st["desc_bytes"] - 1)
     assert status == 7
+
+
+def test_run_pass_checks_before_any_launch(lib):
+    """sp_run_pass reports a node-row count that differs from the plan's
+    (SP_ERR_ARG), a pool smaller than the plan (SP_ERR_POOL_FULL, with the
+    pages needed in the stats) and short descriptor / workspace buffers
+    (SP_ERR_WORKSPACE, with the sizes needed) before anything is enqueued; the
+    device pointers are placeholders that these paths never dereference."""
+    sh = lib.make_shape(8, 2, 64, 16, 64, 100)
+    off, toks = csr([[1, 2, 3, 4], [1, 2, 3, 5]])
+    req = np.zeros(2, np.int32)
+    fake = ctypes.c_void_p(1 << 20)
+
+    def call(node_rows, pool_pages=1 << 20, desc_bytes=1 << 20, attn_ws=1 << 24, lm_ws=1 << 26):
+        st = lib.sp_plan_stats()
+        status = lib.lib().sp_run_pass(
+            ctypes.byref(sh), 2, req.ctypes.data_as(lib._I32P), off.ctypes.data_as(lib._I64P),
+            toks.ctypes.data_as(lib._I32P), node_rows, fake, fake, fake, fake, pool_pages, fake,
+            fake, fake, desc_bytes, fake, attn_ws, fake, fake, fake, fake, 4, fake, fake, fake,
+            lm_ws, fake, fake, None, ctypes.byref(st))
+        return status, st.as_dict()
+
+    status, st = call(4)
+    assert status == 1 and st["node_tokens"] == 5
+    status, st = call(5, pool_pages=2)
+    assert status == 3 and st["pages_used"] == 3
+    status, st = call(5, desc_bytes=16)
+    assert status == 7 and st["desc_bytes"] > 16
+    assert call(5, lm_ws=0)[0] == 7
