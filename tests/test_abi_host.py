@@ -273,3 +273,22 @@ def test_run_pass_checks_before_any_launch(lib):
     status, st = call(5, desc_bytes=16)
     assert status == 7 and st["desc_bytes"] > 16
     assert call(5, lm_ws=0)[0] == 7
+
+
+def test_plain_c_caller(lib, tmp_path):
+    """tests/c_abi_host.c, a C99 program that includes only sp.h and links
+    only libsp, plans two requests, checks their rounds and token accounting,
+    runs the batcher and checks the error codes (host-only entry points)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    libdir = os.path.dirname(lib.lib()._name)
+    exe = tmp_path / "c_abi_host"
+    subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    os.path.join(ROOT, "tests", "c_abi_host.c"), "-L", libdir, "-lsp",
+                    f"-Wl,-rpath,{libdir}", "-o", str(exe)], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stderr
+    assert "passed" in r.stdout
