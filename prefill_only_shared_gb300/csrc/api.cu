@@ -1,5 +1,7 @@
-// C-ABI entry points that touch the GPU: descriptor upload, the two
-// attention calls, the label readout and softmax, and the device error word.
+// C-ABI entry points that touch the GPU: descriptor upload, the three
+// attention calls (prefix, branch, whole tree), the label readout and
+// softmax, the question-type and option decisions, the whole-pass calls
+// (device or host buffers), the bounded flag wait and the device error word.
 // Every argument is validated on the host before anything is launched.
 #include <climits>
 #include <cstring>
