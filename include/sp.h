@@ -16,7 +16,7 @@
  * and is asynchronous: a returned SP_OK means the launch was accepted.
  * sp_run_pass_host also enqueues its input copies on the caller's copy
  * stream, and waits on the host for the previous pass of the input set it
- * is given; sp_check_device_error synchronises its stream. */
+ * is given; sp_check_device_error synchronises its stream.
  *
  * Errors: argument and limit errors are detected on the host BEFORE anything
  * is launched (the article's rule that every rejection happens before
