@@ -450,19 +450,10 @@ def run_libsp(args, ws, rank, local):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16",
-        "data": "synthetic (seeded, BASELINE shapes; random-init LM head)",
-        "config": {
-            "workload": f"{args.config}: Hq {sh.n_q_heads}/Hkv {sh.n_kv_heads}/d {sh.head_dim}, "
-                        f"{N} branches, {stats['logical_tokens']} logical tokens, "
-                        f"{stats['computed_tokens']} computed, H {sh.hidden}, V {sh.vocab}",
-            "branches": N,
-            "branch_tokens_per_step": branch_tokens,
-            "logical_tokens_per_step": stats["logical_tokens"],
-            "rounds": stats["n_rounds"],
-            "l2": "inputs larger than L2 (the 622 MB LM head is streamed every step)",
-            "parallelism": f"replicas x{ws} (independent workloads per GPU)",
-            "attention_schedule": args.schedule,
-        },
+        "data": DATA,
+        "config": workload_config(args.config, sh, N, stats["logical_tokens"],
+                                  stats["computed_tokens"], stats["n_rounds"], branch_tokens, ws,
+                                  args.schedule),
         "other_schedules": {o: {"ms_per_step": round(t, 5),
                                 "value": round(job_value(branch_tokens, ws, t), 1)}
                             for o, t in others.items()},
@@ -602,6 +593,30 @@ def cpu_baseline(wl, config, min_seconds=10.0, max_seconds=30.0):
                       f"full-vocabulary readout and softmax; {dt:.1f} s"}
 
 
+DATA = "synthetic (seeded, the configuration's shapes; random-init LM head)"
+L2_MB = 129  # GB300 L2
+
+
+def workload_config(name, sh, n_branches, logical, computed, n_rounds, branch_tokens, ws,
+                    schedule):
+    """The `config` object of both arms' lines."""
+    w_mb = sh.vocab * sh.hidden * 2 / 1e6
+    return {
+        "workload": f"{name}: Hq {sh.n_q_heads}/Hkv {sh.n_kv_heads}/d {sh.head_dim}, "
+                    f"{n_branches} branches, {logical} logical tokens, {computed} computed, "
+                    f"H {sh.hidden}, V {sh.vocab}",
+        "branches": n_branches,
+        "branch_tokens_per_step": branch_tokens,
+        "logical_tokens_per_step": logical,
+        "rounds": n_rounds,
+        "l2": (f"inputs larger than L2 (the {w_mb:.0f} MB LM head is streamed every step)"
+               if w_mb > L2_MB else
+               f"inputs smaller than L2 ({w_mb:.0f} MB LM head), not flushed: cache-warm figures"),
+        "parallelism": f"replicas x{ws} (independent workloads per GPU)",
+        "attention_schedule": schedule,
+    }
+
+
 def run_reference(args, ws, rank):
     if rank != 0:
         return None
@@ -611,6 +626,9 @@ def run_reference(args, ws, rank):
     from oracle import staging as OS
     wl = make_workload(args.config, seed=0)
     plan = OS.build_plan(wl.req_of_branch, wl.tok_offsets, wl.tokens)
+    ps = OS.plan_stats(plan)
+    branch_tokens = (sum(sg.length for sg in plan.segments if not sg.shared)
+                     + sum(1 for x in plan.recompute if x))
     for i in range(args.warmup):
         oracle_sample(wl, plan, [i % wl.n_branches])
     t = time.perf_counter()
@@ -624,8 +642,10 @@ def run_reference(args, ws, rank):
         "metric": METRIC, "value": round(value, 3), "unit": "branch tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded, BASELINE shapes)",
-        "config": {"workload": args.config, "sample": "1 branch per step"},
+        "data": DATA,
+        "config": workload_config(args.config, wl.shape, wl.n_branches, ps["logical_tokens"],
+                                  ps["computed_tokens"], ps["n_rounds"], branch_tokens, ws,
+                                  args.schedule),
         "cpu_baseline": {"value": round(value, 3), "unit": "branch tokens/s",
                          "cores": os.cpu_count(), "kind": "oracle",
                          "sample": f"{args.config}: 1 branch per step, its suffix rows by "
