@@ -254,3 +254,26 @@ def test_descriptor_tiny_config(lib):
     plan = check(wl.req_of_branch, wl.tok_offsets, wl.tokens, A.to64(wl.q), A.to64(wl.k),
                  A.to64(wl.v), sh.n_q_heads, sh.n_kv_heads, sh.head_dim, lib, 152)
     assert plan.rounds() == [[0], [1, 2, 3]]
+
+
+@pytest.mark.parametrize("n_sms", [1, 8, 152])
+@pytest.mark.parametrize("name", ["tiny", "yesno", "choice64", "tree2"])
+def test_tiles_are_listed_longest_first(lib, name, n_sms):
+    """Blocks start in list order, so every call lists its tiles (and split
+    parts) by non-increasing KV units; paired tiles appear only in calls that
+    are not split."""
+    wl = make_workload(name, tokens_only=True)
+    sh = wl.shape
+    plan = lib.sp_plan_build(lib.make_shape(sh.n_q_heads, sh.n_kv_heads, sh.head_dim, 16,
+                                            sh.hidden, sh.vocab), wl.req_of_branch,
+                             wl.tok_offsets, wl.tokens, 1 << 20, n_sms=n_sms)
+    tiles = decode(plan.descriptor())[4]
+    n_rounds = plan.stats()["n_rounds"]
+    for rnd in list(range(n_rounds)) + [-1]:
+        for kind in (0, 1, 2):
+            ci = plan.call_info(rnd, kind)
+            t = tiles[ci["tile_off"]:ci["tile_off"] + ci["n_tiles"]]
+            units = (t["u_hi"] - t["u_lo"]).astype(np.int64)
+            assert (np.diff(units) <= 0).all(), (rnd, kind)
+            if ci["n_parts"] > 0:
+                assert (t["seg2"] < 0).all(), (rnd, kind)
