@@ -49,6 +49,18 @@ int sm_count() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The host checks of sp_label_logprobs' arguments; the whole-pass calls make
+// them before their first launch.
+sp_status readout_args(const void* h, const void* W, int32_t N, int32_t H, int32_t V,
+                       const int32_t* label_off, const int32_t* label_ids, int32_t n_labels,
+                       const float* logprobs, const float* lse) {
+  if (!h || !W || !label_off || !logprobs || !lse) return SP_ERR_ARG;
+  if (N < 1 || N > 4096 || H < 8 || H % 8 || V < 2 || n_labels < 0) return SP_ERR_ARG;
+  if (n_labels > 0 && !label_ids) return SP_ERR_ARG;
+  if (!aligned16(h) || !aligned16(W)) return SP_ERR_ARG;
+  return SP_OK;
+}
+
 sp_status attn_call(const sp_plan* P, const void* dev_desc, int32_t round, int kind, const void* q,
                     const void* k, const void* v, void* kv_pool, void* out, float* lse,
                     void* workspace, size_t ws_bytes, void* stream) {
@@ -237,10 +249,8 @@ extern "C" sp_status sp_label_logprobs(const void* h, const void* W, int32_t N, 
                                        float* lse, void* workspace, size_t ws_bytes,
                                        void* stream) {
   t_last_launches = 0;
-  if (!h || !W || !label_off || !logprobs || !lse) return SP_ERR_ARG;
-  if (N < 1 || N > 4096 || H < 8 || H % 8 || V < 2 || n_labels < 0) return SP_ERR_ARG;
-  if (n_labels > 0 && !label_ids) return SP_ERR_ARG;
-  if (!aligned16(h) || !aligned16(W)) return SP_ERR_ARG;
+  const sp_status arg = readout_args(h, W, N, H, V, label_off, label_ids, n_labels, logprobs, lse);
+  if (arg != SP_OK) return arg;
   const int n_sms = sm_count();
   const size_t need = sp::lmhead_workspace_bytes(N, V, n_sms);
   if (!workspace || ws_bytes < need || !aligned16(workspace)) return SP_ERR_WORKSPACE;
@@ -433,8 +443,11 @@ extern "C" sp_status sp_run_pass(const sp_shape* shape, int32_t n_branches,
                                    sp_plan_stats* stats) {
   t_last_launches = 0;
   if (!shape || !probs || !argmax) return SP_ERR_ARG;
+  sp_status st = readout_args(h, W, n_branches, shape->hidden, shape->vocab, label_off, label_ids,
+                              n_labels, logprobs, lse_vocab);
+  if (st != SP_OK) return st;
   sp_plan* plan = nullptr;
-  sp_status st = plan_pass(shape, n_branches, req_of_branch, tok_offsets, tokens, node_rows,
+  st = plan_pass(shape, n_branches, req_of_branch, tok_offsets, tokens, node_rows,
                            pool_pages, desc_bytes, attn_ws_bytes, lm_ws_bytes, &plan, stats);
   if (st != SP_OK) return st;
   st = sp_plan_upload(plan, desc, desc_bytes, stream);
@@ -465,6 +478,9 @@ extern "C" sp_status sp_run_pass_host(
     return SP_ERR_ARG;
   if (label_off_host[0] != 0 || label_off_host[n_branches] != n_labels) return SP_ERR_ARG;
   sp_status st = sp_check_labels(label_off_host, label_ids_host, n_branches, shape->vocab);
+  if (st == SP_OK)
+    st = readout_args(set->h, W, n_branches, shape->hidden, shape->vocab, set->label_off,
+                      set->label_ids, n_labels, logprobs, lse_vocab);
   if (st != SP_OK) return st;
   sp_plan* plan = nullptr;
   st = plan_pass(shape, n_branches, req_of_branch, tok_offsets, tokens, node_rows, pool_pages,

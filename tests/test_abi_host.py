@@ -257,14 +257,19 @@ def test_run_pass_checks_before_any_launch(lib):
     req = np.zeros(2, np.int32)
     fake = ctypes.c_void_p(1 << 20)
 
-    def call(node_rows, pool_pages=1 << 20, desc_bytes=1 << 20, attn_ws=1 << 24, lm_ws=1 << 26):
+    def call(node_rows, pool_pages=1 << 20, desc_bytes=1 << 20, attn_ws=1 << 24, lm_ws=1 << 26,
+             h=fake):
         st = lib.sp_plan_stats()
         status = lib.lib().sp_run_pass(
             ctypes.byref(sh), 2, req.ctypes.data_as(lib._I32P), off.ctypes.data_as(lib._I64P),
             toks.ctypes.data_as(lib._I32P), node_rows, fake, fake, fake, fake, pool_pages, fake,
-            fake, fake, desc_bytes, fake, attn_ws, fake, fake, fake, fake, 4, fake, fake, fake,
+            fake, fake, desc_bytes, fake, attn_ws, h, fake, fake, fake, 4, fake, fake, fake,
             lm_ws, fake, fake, None, ctypes.byref(st))
         return status, st.as_dict()
+
+    # the readout's own checks come before the plan too: h not 16-byte aligned
+    status, st = call(5, h=ctypes.c_void_p((1 << 20) + 8))
+    assert status == 1 and st["node_tokens"] == 0
 
     status, st = call(4)
     assert status == 1 and st["node_tokens"] == 5
