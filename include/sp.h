@@ -518,8 +518,9 @@ sp_status sp_option_softmax(const float* row_logprobs, int32_t n_rows, const int
  * the plan needs more than pool_pages pages, SP_ERR_WORKSPACE when desc_bytes,
  * attn_ws_bytes or lm_ws_bytes is short (stats gives desc_bytes and
  * attn_workspace_bytes; nothing is launched then), SP_ERR_ARG when node_rows
- * differs from the plan's node tokens; other errors as for the calls it
- * makes.  The plan lives only inside the call (the descriptor upload stages
+ * differs from the plan's node tokens or when the readout's arguments fail
+ * sp_label_logprobs' checks (those come first, before the plan); other
+ * errors as for the calls it makes.  The plan lives only inside the call (the descriptor upload stages
  * it out of host memory before returning). */
 sp_status sp_run_pass(const sp_shape* shape, int32_t n_branches, const int32_t* req_of_branch,
                       const int64_t* tok_offsets, const int32_t* tokens, int64_t node_rows,
