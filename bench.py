@@ -29,7 +29,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "branch-prefill tokens/s & label decisions/s at 1 GB300; % of roofline"
-DEFAULT_CONFIG = "yesno"
+DEFAULT_CONFIG = "batch64"
 
 
 def parse():

@@ -114,6 +114,44 @@ def reference_attention(plan, q, k, v, branches=None):
     return out, lse, worst
 
 
+def branch_suffix_attention(plan, q, k, v, b: int):
+    """The rows of branch b's own last segment (its suffix), each attending
+    causally over the branch's whole sequence: the last rows of
+    ``causal_attention`` on that sequence, computed for those rows only (the
+    other rows of the sequence are not needed, so a large workload's every
+    suffix row stays affordable).  The query heads of one KV head are stacked
+    into one matrix product per KV head; each score still is q.k / sqrt(d).
+
+    Returns (node rows [S], out [S, Hq, d], lse [S, Hq]).
+    """
+    rows = branch_rows(plan, b)
+    leaf = plan.segments[plan.paths[b][-1]]
+    S = leaf.length
+    L = len(rows)
+    P = L - S
+    qs = to64(q[rows[P:]])                    # [S, Hq, d]
+    kk, vv = to64(k[rows]), to64(v[rows])     # [L, Hkv, d]
+    _, Hq, d = qs.shape
+    Hkv = kk.shape[1]
+    group = Hq // Hkv
+    scale = 1.0 / math.sqrt(d)
+    # query i of the suffix sits at position P + i and sees keys 0 .. P + i
+    future = np.arange(L)[None, :] > (P + np.arange(S))[:, None]          # [S, L]
+    future = np.repeat(future, group, axis=0)                              # [S * group, L]
+    out = np.empty((S, Hq, d))
+    lse = np.empty((S, Hq))
+    for g in range(Hkv):
+        qg = qs[:, g * group:(g + 1) * group, :].reshape(S * group, d)
+        sc = (qg @ kk[:, g, :].T) * scale
+        sc[future] = -np.inf
+        m = sc.max(axis=1, keepdims=True)
+        p = np.exp(sc - m)
+        l = p.sum(axis=1, keepdims=True)
+        out[:, g * group:(g + 1) * group, :] = ((p @ vv[:, g, :]) / l).reshape(S, group, d)
+        lse[:, g * group:(g + 1) * group] = (m[:, 0] + np.log(l[:, 0])).reshape(S, group)
+    return rows[P:], out, lse
+
+
 def sampled_attention(plan, q, k, v, rows):
     """Output rows for selected node-token rows (any size of workload).
 

@@ -131,7 +131,7 @@ EncodeTiledFn get_encode_tiled() {
 namespace {
 struct MapKey {
   const void* base;
-  uint32_t rank, dtype, swz, l2;
+  uint32_t rank, dtype, swz, l2, fill;
   cuuint64_t dims[5];
   cuuint64_t strides[4];
   cuuint32_t box[5];
@@ -146,7 +146,8 @@ constexpr int kMapCache = 32;
 
 bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, const void* base,
                   const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
-                  CUtensorMapSwizzle swz, CUtensorMapL2promotion l2) {
+                  CUtensorMapSwizzle swz, CUtensorMapL2promotion l2,
+                  CUtensorMapFloatOOBfill fill) {
   if (rank < 1 || rank > 5) return false;
   MapKey k;
   std::memset(&k, 0, sizeof(k));
@@ -155,6 +156,7 @@ bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, co
   k.dtype = (uint32_t)dtype;
   k.swz = (uint32_t)swz;
   k.l2 = (uint32_t)l2;
+  k.fill = (uint32_t)fill;
   for (uint32_t i = 0; i < rank; ++i) {
     k.dims[i] = dims[i];
     k.box[i] = box[i];
@@ -171,7 +173,7 @@ bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, co
   if (!enc) return false;
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   if (enc(map, dtype, rank, const_cast<void*>(base), dims, strides, box, estr,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, swz, l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+          CU_TENSOR_MAP_INTERLEAVE_NONE, swz, l2, fill) != CUDA_SUCCESS)
     return false;
   MapEntry& e = cache[next];
   next = (next + 1) % kMapCache;
@@ -283,11 +285,11 @@ extern "C" sp_status sp_label_logprobs_noalloc(const void* h, const void* W, int
                                                const int32_t* label_ids, int32_t n_labels,
                                                float* logprobs, float* lse, void* stream) {
   t_last_launches = 0;
-  if (!h || !W || !label_off || !logprobs || !lse) return SP_ERR_ARG;
-  if (N < 1 || H < 8 || H % 8 || V < 2 || n_labels < 0) return SP_ERR_ARG;
-  if (n_labels > 0 && !label_ids) return SP_ERR_ARG;
-  if (!aligned16(h) || !aligned16(W)) return SP_ERR_ARG;
-  if (N > SP_NOALLOC_MAX_BRANCHES) return SP_ERR_WORKSPACE;
+  const sp_status arg = readout_args(h, W, N, H, V, label_off, label_ids, n_labels, logprobs, lse);
+  if (arg != SP_OK) return arg;
+  const int n_sms = sm_count();
+  // the one size error of this entry point: the static scratch is too small
+  if (!sp::lmhead_noalloc_fits(N, V, n_sms)) return SP_ERR_WORKSPACE;
   sp::LmheadLaunch L;
   L.h = h;
   L.W = W;
@@ -302,14 +304,13 @@ extern "C" sp_status sp_label_logprobs_noalloc(const void* h, const void* W, int
   L.workspace = nullptr;
   L.ws_bytes = 0;
   L.err = error_word_ptr();
-  L.n_sms = sm_count();
+  L.n_sms = n_sms;
   L.stream = stream;
   int launches = 0;
   L.launches = &launches;
   if (!L.err) return SP_ERR_CUDA;
   cudaError_t e = sp::lmhead_run_noalloc(L);
   t_last_launches = launches;
-  if (e == cudaErrorInvalidValue) return SP_ERR_WORKSPACE;
   return e == cudaSuccess ? SP_OK : SP_ERR_CUDA;
 }
 

@@ -85,6 +85,12 @@ struct AttnArgs {
   unsigned* err;
   int Hq, Hkv, G;
   float scale_log2;  // log2(e) / sqrt(d)
+  // bounds of the descriptor's indices, checked on the device: rows of the
+  // q / k / v / out inputs, pages of the pool, page-table entries, partial slots
+  int64_t node_tokens;
+  int64_t pool_pages;
+  int64_t n_page_entries;
+  int32_t n_parts;
 };
 
 // MN-major operand, 128-byte swizzle (V as the B operand of P.V: rows are
@@ -478,11 +484,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       walk.start(a, sd, td);
       int page = 0;
       bool in_seg = false;
+      // A level read from the pool names its pages through the page table.  A
+      // page-table index or a page id out of range (a stale or mismatched
+      // descriptor) sets the bounds bit of the error word; the fetch then
+      // reads outside the pool tensor, which the pool maps fill with NaN, so
+      // the rows that use it come out NaN and nothing outside the pool is read.
       auto fetch_page = [&](const Cursor& c) {
         int pi = c.j * kPages + lane;
         in_seg = pi < c.n_pages;
         if (!in_seg) pi = c.n_pages - 1;  // finite filler; its keys are masked
-        page = a.page_ids[c.page_off + pi];
+        const int64_t e = (int64_t)c.page_off + pi;
+        page = e >= 0 && e < a.n_page_entries ? a.page_ids[e] : -1;
+        if (!c.local && (page < 0 || (int64_t)page >= a.pool_pages)) {
+          raise_error(a.err, kErrBounds);
+          page = -1;
+        }
       };
       if (lane < kPages) fetch_page(walk.cur);
       int s = 0;
@@ -539,6 +555,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // segment's last token zero-fills the rest of that page.  No tile of
       // this call reads these pages.
       if (ok && td.u_lo == 0 && sd.shared == 1 && computed_here(a, sd)) {
+        // a page id or a source row out of range skips its store and sets the
+        // bounds bit of the error word
         constexpr int kChunks = D / 8;  // 16-byte chunks per row
         const bf16* src = is_k ? a.k_in : a.v_in;
         const size_t page_elems = (size_t)2 * a.Hkv * kPageSize * D;
@@ -554,16 +572,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int i = i0 + b * 32 + lane;
             const int t = td.t0 + i / kChunks, ch = i % kChunks;
             val[b] = make_uint4(0, 0, 0, 0);
-            if (i < n_items && t < t_end)
-              val[b] = *reinterpret_cast<const uint4*>(
-                  src + ((size_t)(sd.node_start + t) * a.Hkv + hkv) * D + ch * 8);
+            if (i < n_items && t < t_end) {
+              const int64_t row = sd.node_start + t;
+              if (row >= 0 && row < a.node_tokens)
+                val[b] = *reinterpret_cast<const uint4*>(src + ((size_t)row * a.Hkv + hkv) * D + ch * 8);
+              else
+                raise_error(a.err, kErrBounds);
+            }
           }
 #pragma unroll
           for (int b = 0; b < kBatch; ++b) {
             const int i = i0 + b * 32 + lane;
             if (i >= n_items) break;
             const int t = td.t0 + i / kChunks, ch = i % kChunks;
-            const int page = a.page_ids[sd.page_off + t / kPageSize];
+            const int64_t e = (int64_t)sd.page_off + t / kPageSize;
+            const int page = e >= 0 && e < a.n_page_entries ? a.page_ids[e] : -1;
+            if (page < 0 || (int64_t)page >= a.pool_pages) {
+              raise_error(a.err, kErrBounds);
+              continue;
+            }
             *reinterpret_cast<uint4*>(a.pool + (size_t)page * page_elems + kv_off +
                                       (size_t)(t % kPageSize) * D + ch * 8) = val[b];
           }
@@ -745,14 +772,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool pair_b = h == 1 && td.seg2 >= 0;
       const int nt_h = h == 0 ? min(td.nt, kHalf / G) : pair_b ? td.ntb : td.nt - kHalf / G;
       const int64_t seg_row0 = pair_b ? a.segs[td.seg2].node_start : sd.node_start;
-      const bool row_ok = tok < nt_h;
+      // a row or a partial slot out of range (a bad descriptor) is not
+      // written and sets the bounds bit of the error word
+      const bool in_range = td.part < 0 ? seg_row0 + token >= 0 && seg_row0 + token < a.node_tokens
+                                        : td.part < a.n_parts;
+      if (tok < nt_h && !in_range) raise_error(a.err, kErrBounds);
+      const bool row_ok = tok < nt_h && in_range;
       const int head = hkv * G + (r % G);
       const size_t orow = (size_t)(seg_row0 + token) * a.Hq + head;
       const size_t prow_i = ((size_t)td.part * a.Hkv + hkv) * kRowsPerTile + h * kHalf + r;
       // A final half whose rows are all tokens of the tile goes out through
       // the Q_h buffer (its products are done) and TMA stores: rows laid out
       // like the Q box (token x head), 128-byte swizzled.
-      const bool staged = td.part < 0 && nt_h >= kHalf / G;
+      // (TMA stores start only inside the output: a store must not start at
+      // a negative row, so a half whose rows fall outside goes the checked way)
+      const int64_t half_row0 = seg_row0 + (token - tok);
+      const bool staged = td.part < 0 && nt_h >= kHalf / G && half_row0 >= 0 &&
+                          half_row0 + kHalf / G <= a.node_tokens;
       unsigned char* stage = sQ + h * C::kQHalf;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
@@ -799,8 +835,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if ((warp & 3) == 0 && lane == 0) {
           if (mbar_wait(&stage_full[h], 0, abort_flag)) {
             for (int slab = 0; slab < D / 64; ++slab)
-              tma_store_3d(&tmO, stage + slab * C::kQSlab, slab * 64, hkv * G,
-                           (int32_t)(seg_row0 + token - tok));
+              tma_store_3d(&tmO, stage + slab * C::kQSlab, slab * 64, hkv * G, (int32_t)half_row0);
             bulk_commit_and_wait_read();  // the smem stays valid until the stores read it
           } else {
             if (!*abort_flag) raise_error(a.err, kErrTimeout);
@@ -832,7 +867,8 @@ template <int D>
 __global__ void __launch_bounds__(256) attn_merge_kernel(const SegDesc* segs, const MergeDesc* merges,
                                                          const float* part_o, const float* part_lse,
                                                          bf16* out, float* lse_out, int Hq, int Hkv,
-                                                         int G) {
+                                                         int G, int64_t node_tokens, int n_parts,
+                                                         unsigned* err) {
   constexpr int PER = D / 32;
   constexpr int kBatch = 8;
   const MergeDesc md = merges[blockIdx.x >> 5];
@@ -840,6 +876,14 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const SegDesc* segs, co
   const int row = (blockIdx.x & 31) * 8 + warp;
   const int hkv = blockIdx.y;
   if (row / G >= md.nt) return;
+  // partial slots and the output row inside their buffers, else the bounds
+  // bit of the error word and nothing read or written
+  const int64_t out_row = segs[md.seg].node_start + md.t0 + row / G;
+  if (md.part0 < 0 || md.nparts < 0 || (int64_t)md.part0 + md.nparts > n_parts || out_row < 0 ||
+      out_row >= node_tokens) {
+    if (lane == 0) raise_error(err, kErrBounds);
+    return;
+  }
   const size_t step = (size_t)Hkv * kRowsPerTile;
   const size_t base = ((size_t)md.part0 * Hkv + hkv) * kRowsPerTile + row;
   float M = -INFINITY;
@@ -878,8 +922,7 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const SegDesc* segs, co
     }
   }
   const float inv = S > 0.f ? 1.f / S : 0.f;
-  const SegDesc sd = segs[md.seg];
-  const size_t orow = (size_t)(sd.node_start + md.t0 + row / G) * Hq + hkv * G + (row % G);
+  const size_t orow = (size_t)out_row * Hq + hkv * G + (row % G);
 #pragma unroll
   for (int e = 0; e < PER; e += 2)
     *reinterpret_cast<uint32_t*>(out + orow * D + lane * PER + e) =
@@ -888,9 +931,10 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const SegDesc* segs, co
 }
 
 bool encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
-            const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swz) {
+            const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swz,
+            CUtensorMapFloatOOBfill fill = CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) {
   return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (uint32_t)rank, base, dims, strides,
-                      box, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+                      box, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, fill);
 }
 
 template <int D>
@@ -928,6 +972,7 @@ cudaError_t run_call(const AttnLaunch& L) {
         return cudaErrorInvalidValue;
     }
     // pool page: [K: Hkv][16][D] then [V: Hkv][16][D]; dims (inner first)
+    constexpr CUtensorMapFloatOOBfill kNanFill = CU_TENSOR_MAP_FLOAT_OOB_FILL_NAN_REQUEST_ZERO_FMA;
     const cuuint64_t page_bytes = (cuuint64_t)2 * L.Hkv * kPageSize * D * 2;
     {
       cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)kPageSize, (cuuint64_t)L.Hkv,
@@ -935,8 +980,9 @@ cudaError_t run_call(const AttnLaunch& L) {
       cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)kPageSize * D * 2, page_bytes};
       cuuint32_t boxr[4] = {64, (cuuint32_t)kPageSize, 1, (cuuint32_t)kPages};
       cuuint32_t box1[4] = {64, (cuuint32_t)kPageSize, 1, 1};
-      if (!encode(&tmKr, pool, 4, dims, strides, boxr, CU_TENSOR_MAP_SWIZZLE_128B) ||
-          !encode(&tmK1, pool, 4, dims, strides, box1, CU_TENSOR_MAP_SWIZZLE_128B))
+      // a valid descriptor never reads outside the plan's pages: NaN there
+      if (!encode(&tmKr, pool, 4, dims, strides, boxr, CU_TENSOR_MAP_SWIZZLE_128B, kNanFill) ||
+          !encode(&tmK1, pool, 4, dims, strides, box1, CU_TENSOR_MAP_SWIZZLE_128B, kNanFill))
         return cudaErrorInvalidValue;
     }
     {
@@ -946,8 +992,8 @@ cudaError_t run_call(const AttnLaunch& L) {
       cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)kPageSize * D * 2, page_bytes};
       cuuint32_t boxr[4] = {64, (cuuint32_t)kPageSize, 1, (cuuint32_t)kPages};
       cuuint32_t box1[4] = {64, (cuuint32_t)kPageSize, 1, 1};
-      if (!encode(&tmVr, vbase, 4, dims, strides, boxr, CU_TENSOR_MAP_SWIZZLE_128B) ||
-          !encode(&tmV1, vbase, 4, dims, strides, box1, CU_TENSOR_MAP_SWIZZLE_128B))
+      if (!encode(&tmVr, vbase, 4, dims, strides, boxr, CU_TENSOR_MAP_SWIZZLE_128B, kNanFill) ||
+          !encode(&tmV1, vbase, 4, dims, strides, box1, CU_TENSOR_MAP_SWIZZLE_128B, kNanFill))
         return cudaErrorInvalidValue;
     }
     AttnArgs a;
@@ -969,6 +1015,10 @@ cudaError_t run_call(const AttnLaunch& L) {
     a.Hkv = L.Hkv;
     a.G = G;
     a.scale_log2 = 1.4426950408889634f / sqrtf((float)D);
+    a.node_tokens = L.node_tokens;
+    a.pool_pages = L.pool_pages;
+    a.n_page_entries = h.n_pages;
+    a.n_parts = L.n_parts;
     const size_t smem = Cfg<D>::kSmem;
     cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(attn_tc_kernel<D>), (int)smem);
     if (e != cudaSuccess) return e;
@@ -980,7 +1030,8 @@ cudaError_t run_call(const AttnLaunch& L) {
   if (L.n_merges > 0) {
     dim3 grid((unsigned)L.n_merges * 32, (unsigned)L.Hkv);
     attn_merge_kernel<D><<<grid, 256, 0, st>>>(segs, merges, part_o, part_lse,
-                                               static_cast<bf16*>(L.out), L.lse, L.Hq, L.Hkv, G);
+                                               static_cast<bf16*>(L.out), L.lse, L.Hq, L.Hkv, G,
+                                               L.node_tokens, L.n_parts, L.err);
     ++launches;
   }
   *L.launches = launches;

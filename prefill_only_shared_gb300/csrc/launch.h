@@ -55,9 +55,13 @@ size_t lmhead_workspace_bytes(int N, int V, int n_sms);
 cudaError_t lmhead_run(const LmheadLaunch& L);
 
 // The readout with its scratch in the library's static device array (no
-// allocation); N <= kNoallocMaxBranches.
+// allocation): up to kNoallocMaxCtas x kNoallocMaxBranches partial pairs, then
+// the two counters.  The caller checks lmhead_noalloc_fits first.
 constexpr int kNoallocMaxBranches = 1024;
 constexpr int kNoallocMaxCtas = 256;
+constexpr size_t kNoallocScratchBytes =
+    (size_t)kNoallocMaxCtas * kNoallocMaxBranches * 8 /* float2 */ + 256;
+bool lmhead_noalloc_fits(int N, int V, int n_sms);
 cudaError_t lmhead_run_noalloc(LmheadLaunch L);
 
 cudaError_t label_softmax_run(const float* logprobs, const int32_t* label_off, int N, float* probs,
@@ -88,11 +92,14 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn get_encode_tiled();
 
-// cuTensorMapEncodeTiled with element strides 1, no interleave, no OOB fill
-// override, through a per-thread cache of recent encodings.
+// cuTensorMapEncodeTiled with element strides 1 and no interleave, through a
+// per-thread cache of recent encodings.  `fill`: what a load reads outside
+// the tensor (zeros by default; NaN for maps whose out-of-range reads can
+// only come from a bad descriptor, so such reads poison the results).
 bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, const void* base,
                   const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
-                  CUtensorMapSwizzle swz, CUtensorMapL2promotion l2);
+                  CUtensorMapSwizzle swz, CUtensorMapL2promotion l2,
+                  CUtensorMapFloatOOBfill fill = CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 
 // Raise a kernel's dynamic shared memory limit, once per kernel and device.
 cudaError_t ensure_dynamic_smem(const void* func, int bytes);

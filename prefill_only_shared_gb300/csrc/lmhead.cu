@@ -26,6 +26,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "sp.h"
 
 namespace sp {
 namespace {
@@ -552,9 +553,12 @@ cudaError_t lmhead_run(const LmheadLaunch& L) {
 // that device current) and passed to the kernel like any workspace.  Calls
 // share the array; each call writes every partial it reads, so nothing needs
 // clearing, and overlapping calls would race.
+static_assert(SP_NOALLOC_SCRATCH_BYTES == kNoallocScratchBytes,
+              "the header's scratch size must be the array's");
+static_assert(SP_NOALLOC_MAX_BRANCHES == kNoallocMaxBranches,
+              "the header's branch limit must be the library's");
+static_assert(sizeof(float2) == 8, "one partial pair is 8 bytes");
 namespace {
-constexpr size_t kNoallocScratchBytes =
-    (size_t)kNoallocMaxCtas * kNoallocMaxBranches * sizeof(float2) + 256;  // + the counters
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
 cudaError_t noalloc_scratch_address(void** out) {
@@ -577,10 +581,16 @@ cudaError_t noalloc_scratch_address(void** out) {
 }
 }  // namespace
 
+bool lmhead_noalloc_fits(int N, int V, int n_sms) {
+  if (N < 1 || N > kNoallocMaxBranches) return false;
+  if (n_sms > kNoallocMaxCtas) n_sms = kNoallocMaxCtas;
+  return lmhead_workspace_bytes(N, V, n_sms) <= kNoallocScratchBytes;
+}
+
 cudaError_t lmhead_run_noalloc(LmheadLaunch L) {
-  if (L.N > kNoallocMaxBranches) return cudaErrorInvalidValue;
-  if (L.n_sms > kNoallocMaxCtas) L.n_sms = kNoallocMaxCtas;  // caps the grid, hence the partials
-  if (lmhead_workspace_bytes(L.N, L.V, L.n_sms) > kNoallocScratchBytes) return cudaErrorInvalidValue;
+  // the grid is capped so the partials fit the array (checked by the caller
+  // through lmhead_noalloc_fits with the same cap)
+  if (L.n_sms > kNoallocMaxCtas) L.n_sms = kNoallocMaxCtas;
   void* scratch = nullptr;
   cudaError_t e = noalloc_scratch_address(&scratch);
   if (e != cudaSuccess) return e;

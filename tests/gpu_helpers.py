@@ -109,3 +109,18 @@ def check_attention_sampled(wl, g, n_random=64, seed=0):
     assert np.abs(g["out"][rows] - so).max() <= TOL_OUT
     assert np.abs(g["lse"][rows] - sl).max() <= TOL_LSE
     return plan, rows
+
+
+def check_attention_suffix_rows(wl, g, branches=None):
+    """Every row of each branch's own last segment (its suffix, the branch
+    tokens the metric counts) against unshared float64 attention over the
+    branch's whole sequence."""
+    plan = OS.build_plan(wl.req_of_branch, wl.tok_offsets, wl.tokens)
+    worst_o = worst_l = 0.0
+    for b in (range(len(plan.paths)) if branches is None else branches):
+        rows, o, l = OA.branch_suffix_attention(plan, wl.q, wl.k, wl.v, b)
+        worst_o = max(worst_o, float(np.abs(g["out"][rows] - o).max()))
+        worst_l = max(worst_l, float(np.abs(g["lse"][rows] - l).max()))
+    assert worst_o <= TOL_OUT, worst_o
+    assert worst_l <= TOL_LSE, worst_l
+    return worst_o, worst_l

@@ -10,7 +10,7 @@ from oracle import staging as OS
 from prefill_only_shared_gb300.workloads import make_workload, small_case
 
 from gpu_helpers import (TOL_LSE, TOL_OUT, check_attention_full, check_attention_sampled,
-                         check_readout, run_gpu)
+                         check_attention_suffix_rows, check_readout, run_gpu)
 
 pytestmark = pytest.mark.gpu
 
@@ -111,8 +111,9 @@ def test_full_size_configs(cuda_dev, lib, name, schedule):
                 "choice64": [[0], list(range(1, 64))]}[name]
     assert g["rounds"] == expected
     check_attention_sampled(wl, g, n_random=96)
-    branches = None if wl.n_branches <= 8 else [0, 1, 2, 17, 33, 62, 63]
-    check_readout(wl, g, branches)
+    # every branch: all of its suffix rows, its readout, softmax and argmax
+    check_attention_suffix_rows(wl, g)
+    check_readout(wl, g)
 
 
 @pytest.mark.parametrize("schedule", ["rounds", "tree"])
@@ -121,7 +122,13 @@ def test_full_size_batch64(cuda_dev, lib, schedule):
     g = run_gpu(wl, schedule=schedule)
     assert len(g["rounds"]) == 2 and len(g["rounds"][0]) == 64
     check_attention_sampled(wl, g, n_random=128)
-    check_readout(wl, g, [0, 1, 11, 12, 100, 383, 500, 767])
+    if schedule == "tree":
+        # the bench's schedule: every one of the 768 branches, all 49152 suffix
+        # rows and every readout, softmax and argmax
+        check_attention_suffix_rows(wl, g)
+        check_readout(wl, g)
+    else:
+        check_readout(wl, g, [0, 1, 11, 12, 100, 383, 500, 767])
     if schedule == "tree":
         _CACHE.pop("batch64", None)
 

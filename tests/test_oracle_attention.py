@@ -124,3 +124,31 @@ def test_prefix_free_sequence_is_plain_causal():
     out, _, _ = A.reference_attention(plan, wl.q, wl.k, wl.v)
     ob, _ = brute_force(A.to64(wl.q), A.to64(wl.k), A.to64(wl.v))
     assert np.abs(out - ob).max() < 1e-12
+
+
+def test_branch_suffix_rows_match_brute_force_and_sdpa():
+    """Every branch's suffix rows, computed for those rows alone, equal the
+    scalar brute force over the branch's whole sequence (small tree) and
+    torch's float64 SDPA over it (a larger GQA tree)."""
+    from prefill_only_shared_gb300.workloads import small_case
+    wl = small_case((6, [(4, [(3, []), (2, [])]), (5, [])]), n_q_heads=4, n_kv_heads=2, head_dim=8)
+    plan = S.build_plan(wl.req_of_branch, wl.tok_offsets, wl.tokens)
+    for b in range(len(plan.paths)):
+        rows = A.branch_rows(plan, b)
+        ob, lb = brute_force(A.to64(wl.q[rows]), A.to64(wl.k[rows]), A.to64(wl.v[rows]))
+        srows, o, l = A.branch_suffix_attention(plan, wl.q, wl.k, wl.v, b)
+        n = len(srows)
+        assert (srows == rows[-n:]).all()
+        assert np.abs(o - ob[-n:]).max() < 1e-12
+        assert np.abs(l - lb[-n:]).max() < 1e-12
+    wl = small_case((70, [(33, []), (9, [(20, []), (1, [])])]), n_q_heads=16, n_kv_heads=2,
+                    head_dim=32)
+    plan = S.build_plan(wl.req_of_branch, wl.tok_offsets, wl.tokens)
+    for b in range(len(plan.paths)):
+        rows = A.branch_rows(plan, b)
+        qb, kb, vb = (torch.from_numpy(A.to64(t[rows])) for t in (wl.q, wl.k, wl.v))
+        ref = F.scaled_dot_product_attention(
+            qb.transpose(0, 1)[None], kb.transpose(0, 1)[None], vb.transpose(0, 1)[None],
+            is_causal=True, enable_gqa=True)[0].transpose(0, 1).numpy()
+        srows, o, _ = A.branch_suffix_attention(plan, wl.q, wl.k, wl.v, b)
+        assert np.abs(o - ref[-len(srows):]).max() < 1e-12
