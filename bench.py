@@ -46,6 +46,9 @@ def parse():
                          "pair of calls per round (same work and results)")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the oracle timing (short profiling runs)")
+    ap.add_argument("--only", default="all", choices=["all", "attention", "readout"],
+                    help="profiling runs: time one phase of the step alone (only its inputs "
+                         "on the device) and print its timing line instead of the bench line")
     return ap.parse_args()
 
 
@@ -77,6 +80,9 @@ def job_value(units_per_rank, ws, ms_per_step):
 # --------------------------------------------------------------------------
 # clocks sampled during the timed region
 class ClockSampler:
+    """nvidia-smi samples every 100 ms on a reader thread, each stamped with
+    the host time it arrived; the summary keeps the samples between mark()
+    (the start of the timed region, after the warm-up) and stop()."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -85,6 +91,7 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.lines = []
+        self.t_mark = 0.0
 
     def start(self):
         try:
@@ -97,11 +104,15 @@ class ClockSampler:
         except Exception:
             self.proc = None
 
+    def mark(self):
+        self.t_mark = time.time()
+
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
 
     def stop(self):
+        t_stop = time.time()
         if not self.proc:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -110,9 +121,13 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.t.join(timeout=2)
-        sm, mx, reasons = [], None, set()
+        sm, pw, mx, reasons = [], [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        window = [ln for t, ln in self.lines if self.t_mark <= t <= t_stop + 0.15]
+        if not window:  # a timed region shorter than one sample: the nearest sample
+            after = [ln for t, ln in self.lines if t >= self.t_mark]
+            window = after[:1] or [ln for _, ln in self.lines[-1:]]
+        for ln in window:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -121,11 +136,16 @@ class ClockSampler:
                 mx = float(parts[2])
             except ValueError:
                 continue
+            try:
+                pw.append(float(parts[3]))
+            except ValueError:
+                pass
             for nm, val in zip(names, parts[5:9]):
                 if val.lower().startswith("active"):
                     reasons.add(nm)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_median": statistics.median(pw) if pw else None}
 
 
 def load_peaks():
@@ -138,8 +158,8 @@ def load_peaks():
 
 def kernel_traffic(kernel_file: str, config: str):
     """DRAM bytes per launch from the committed ncu summary
-    (profiles/traffic_<kernel>_<config>.txt), if the kernel source is unchanged
-    since it was captured; else None."""
+    (profiles/traffic_<kernel file>_<config>.txt), if the kernel source is
+    unchanged since it was captured; else None."""
     src = os.path.join(ROOT, "prefill_only_shared_gb300", "csrc", kernel_file)
     summ = os.path.join(ROOT, "profiles", f"traffic_{os.path.splitext(kernel_file)[0]}_{config}.txt")
     if not (os.path.exists(src) and os.path.exists(summ)):
@@ -197,6 +217,8 @@ def run_libsp(args, ws, rank, local):
     sh = wl.shape
     clf = SharedPrefixClassifier(sh.n_q_heads, sh.n_kv_heads, sh.head_dim, sh.hidden, sh.vocab,
                                  device=dev)
+    if args.only != "all":
+        return run_phase(args, wl, clf, dev) if rank == 0 else None
     q, k, v = wl.q.to(dev), wl.k.to(dev), wl.v.to(dev)
     h, W = wl.h.to(dev), wl.W.to(dev)
     off = torch.from_numpy(wl.label_off).to(dev)
@@ -226,6 +248,7 @@ def run_libsp(args, ws, rank, local):
     sp.sp_check_device_error()
     stats = plan.stats()
     segs = plan.segments()
+    attn_launches = clf.last_attention_launches
     launches_per_step = clf.last_attention_launches + clf.last_logprob_launches + \
         clf.last_softmax_launches
     branch_tokens = int(sum(segs["len"][i] for i in range(len(segs["len"])) if not segs["shared"][i]))
@@ -246,6 +269,7 @@ def run_libsp(args, ws, rank, local):
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    sampler.mark()
     t_start.record(stream)
     for i in range(args.steps):
         step(evs[i])
@@ -438,6 +462,36 @@ def run_libsp(args, ws, rank, local):
         achieved = lm_bytes / (lm_avg / 1e3) / 1e9
         lm_peak, lm_unit, lm_peak_key = peaks["hbm_gbs"], "GB/s", "hbm_gbs"
     attn_flops = f_prefix + f_branch
+    attn_peak_key = "bf16_tflops_sustained" if "bf16_tflops_sustained" in peaks else "bf16_tflops"
+    attn_achieved = attn_flops / (attn_avg / 1e3) / 1e12
+    readout_roofline = {
+        "kernel": "lmhead_kernel (the whole sp_label_logprobs call: barrier-counter memset + one cooperative launch)",
+        "bound": "tensor" if lm_tensor else "hbm",
+        "achieved": round(achieved, 1),
+        "peak": lm_peak,
+        "unit": lm_unit,
+        "frac": round(achieved / lm_peak, 4),
+        "traffic": kernel_traffic("lmhead.cu", args.config),
+        "peak_source": f"{peak_kind} {lm_peak_key}",
+        "algorithmic_bytes_per_launch": lm_bytes,
+        "algorithmic_flops_per_launch": lm_flops,
+    }
+    attention_roofline = {
+        "kernel": f"attn_tc_kernel (the whole attention of a step: {attn_launches} "
+                  f"launch(es) of the {args.schedule} schedule)",
+        "bound": "tensor",
+        "achieved": round(attn_achieved, 2),
+        "peak": peaks[attn_peak_key],
+        "unit": "TFLOP/s",
+        "frac": round(attn_achieved / peaks[attn_peak_key], 4),
+        "traffic": kernel_traffic("attn.cu", args.config),
+        "peak_source": f"{peak_kind} {attn_peak_key}",
+        "algorithmic_flops_per_launch": attn_flops,
+        "note": "the attention calls of a step incl. KV append and merges",
+    }
+    # the headline roofline is the dominant kernel's: the phase with the
+    # larger share of the step
+    dominant = "attention" if attn_avg >= lm_avg else "readout"
     result = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -515,28 +569,9 @@ def run_libsp(args, ws, rank, local):
         "phase_ms": {"attention": round(attn_avg, 5), "label_logprobs": round(lm_avg, 5),
                      "label_softmax": round(statistics.mean(sm_ms), 5),
                      "plan_and_launch_overhead": round(ms - attn_avg - lm_avg - statistics.mean(sm_ms), 5)},
-        "roofline": {
-            "kernel": "lmhead_kernel (the whole sp_label_logprobs call: barrier-counter memset + one cooperative launch)",
-            "bound": "tensor" if lm_tensor else "hbm",
-            "achieved": round(achieved, 1),
-            "peak": lm_peak,
-            "unit": lm_unit,
-            "frac": round(achieved / lm_peak, 4),
-            "traffic": kernel_traffic("lmhead.cu", args.config),
-            "peak_source": f"{peak_kind} {lm_peak_key}",
-            "algorithmic_bytes_per_launch": lm_bytes,
-            "algorithmic_flops_per_launch": lm_flops,
-        },
-        "attention_roofline": {
-            "bound": "tensor",
-            "achieved": round(attn_flops / (attn_avg / 1e3) / 1e12, 2),
-            "peak": peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]),
-            "unit": "TFLOP/s",
-            "frac": round(attn_flops / (attn_avg / 1e3) / 1e12 /
-                          peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]), 4),
-            "algorithmic_flops_per_step": attn_flops,
-            "note": "all attention calls of a step incl. KV append and merges",
-        },
+        "roofline": dict(attention_roofline if dominant == "attention" else readout_roofline),
+        "attention_roofline": attention_roofline,
+        "readout_roofline": readout_roofline,
         "e2e": {"value": round(branch_tokens * ws / (e2e_ms / 1e3), 1), "unit": "branch tokens/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "ms_per_step": round(e2e_ms, 5)},
@@ -548,6 +583,54 @@ def run_libsp(args, ws, rank, local):
     if ws > 1:
         torch.distributed.destroy_process_group()
     return result if rank == 0 else None
+
+
+def run_phase(args, wl, clf, dev):
+    """One phase of the step alone, for kernel profiles on a small device
+    footprint: "attention" holds q / k / v and the pool; "readout" holds h, W
+    and the labels (the readout and the label softmax).  Returns a timing line
+    (CUDA events around each call, after the warm-up calls)."""
+    import torch
+    from prefill_only_shared_gb300 import sp
+    stream = torch.cuda.current_stream(dev)
+    sh = wl.shape
+    N = wl.n_branches
+    if args.only == "attention":
+        q, k, v = wl.q.to(dev), wl.k.to(dev), wl.v.to(dev)
+        plan = clf.plan(wl.req_of_branch, wl.tok_offsets, wl.tokens)
+        call = lambda: clf.attention(plan, q, k, v, stream, args.schedule)
+        f_prefix, f_branch = attention_flops(plan.segments(), wl)
+        work = {"flops_per_call": f_prefix + f_branch}
+    else:
+        h, W = wl.h.to(dev), wl.W.to(dev)
+        off = torch.from_numpy(wl.label_off).to(dev)
+        ids = torch.from_numpy(wl.label_ids).to(dev)
+        n_labels = int(wl.label_ids.shape[0])
+
+        def call():
+            lp, _ = clf.logprobs(h, W, off, ids, n_labels, stream)
+            clf.softmax(lp, off, stream)
+        work = {"flops_per_call": 2.0 * N * sh.hidden * sh.vocab,
+                "bytes_per_call": sh.vocab * sh.hidden * 2 + N * sh.hidden * 2 + n_labels * 8 + N * 4}
+    for _ in range(max(args.warmup, 1)):
+        call()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.3)
+    sampler.mark()
+    for e0, e1 in evs:
+        e0.record(stream)
+        call()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    sp.sp_check_device_error()
+    ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
+    return {"phase": args.only, "config": args.config, "schedule": args.schedule,
+            "calls": args.steps, "ms_per_call_median": round(ms, 5), **work, "clocks": clocks}
 
 
 # --------------------------------------------------------------------------

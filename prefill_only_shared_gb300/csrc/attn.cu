@@ -401,8 +401,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* v_empty = v_full + kVStages;
   uint64_t* s_full = v_empty + kVStages;  // [2]: S_h of the current unit is in TMEM
   uint64_t* p_full = s_full + 2;          // [2]: P_h of the current unit is in TMEM
-  uint64_t* o_full = p_full + 2;          // [2]: all products of half h done
-  uint64_t* first_turn = o_full + 2;      // half A issued its first group
+  uint64_t* o_full = p_full + 2;          // [2]: all products of half h done, O_h complete
+  uint64_t* drain = o_full + 2;           // [2]: the products half h issued before it gave up
+  uint64_t* first_turn = drain + 2;       // half A issued its first group
   uint64_t* stage_full = first_turn + 1;  // [2]: half h's output rows are staged in smem
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stage_full + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -438,6 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s_full[h], 1);
       mbar_init(&p_full[h], 4u + (n_halves == 2 ? 1u : 0u));
       mbar_init(&o_full[h], 1);
+      mbar_init(&drain[h], 1);
     }
     mbar_init(first_turn, 1);
     mbar_init(&stage_full[0], 4);
@@ -542,9 +544,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           ph ^= 1;
         }
       }
-      if (!ok && lane == 0) {
-        if (!*abort_flag) raise_error(a.err, kErrTimeout);
-        *abort_flag = 1;
+      if (lane == 0) {
+        if (!ok) {
+          if (!*abort_flag) raise_error(a.err, kErrTimeout);
+          *abort_flag = 1;
+        }
+        // every load issued has landed before the CTA exits: after an abort
+        // the issuers may not have read them all (on the normal path they
+        // have, and these waits end at once)
         if (is_k) mbar_wait(q_full, 0, nullptr);
         for (int i = 0; i < n_st; ++i)
           if (issued[i] >= 0) mbar_wait(&full[i], (uint32_t)issued[i], nullptr);
@@ -666,12 +673,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (!ok) {
+      if (ok) {
+        umma_commit(&o_full[h]);  // every product of this half: O_h is complete
+        mbar_wait(&o_full[h], 0, nullptr);
+      } else {
+        // gave up: o_full stays incomplete (the softmax sees the abort flag
+        // instead), and the products issued so far finish before the exit
         if (!*abort_flag) raise_error(a.err, kErrTimeout);
         *abort_flag = 1;
+        umma_commit(&drain[h]);
+        mbar_wait(&drain[h], 0, nullptr);
       }
-      umma_commit(&o_full[h]);  // every product of this half, also on the abort path
-      mbar_wait(&o_full[h], 0, nullptr);
     }
   } else if (warp < 8 && n_units > 0 && (warp < 4 || has_b)) {
     // ---------------- softmax / epilogue of one half ----------------
@@ -766,8 +778,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       *abort_flag = 1;
     } else {
       tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      const float lse = l > 0.f ? (m_used + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+      // (a NaN sum, from a NaN key or value, stays NaN in both)
+      const float inv = l == 0.f ? 0.f : 1.f / l;
+      const float lse = l == 0.f ? -INFINITY : (m_used + __log2f(l)) * 0.69314718055994531f;
       // half h's rows: tokens of its segment from seg_row0 on, nt_h of them
       const bool pair_b = h == 1 && td.seg2 >= 0;
       const int nt_h = h == 0 ? min(td.nt, kHalf / G) : pair_b ? td.ntb : td.nt - kHalf / G;

@@ -145,7 +145,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer ----------------
-    const uint64_t pol_w = l2_policy_evict_first();
+    // W is streamed once: evict-first, except that a vocab tile read again
+    // by the next branch chunk (its units are consecutive) stays in L2 until
+    // its last chunk reads it
+    const uint64_t pol_first = l2_policy_evict_first();
+    const uint64_t pol_keep = l2_policy_evict_last();
     const uint64_t pol_h = l2_policy_evict_last();
     int s = 0;
     uint32_t ph = 0;
@@ -169,6 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&unit_full[r]);  // releases the write above
       if (u < 0) break;
       const int t = u / a.n_ch, c = u % a.n_ch;
+      const uint64_t pol_w = c == a.n_ch - 1 ? pol_first : pol_keep;
       for (int k = 0; k < nk; ++k) {
         if (!mbar_wait(&empty[s], ph ^ 1, abort_flag)) {
           ok = false;
@@ -188,10 +193,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok) {
       if (!*abort_flag) raise_error(a.err, kErrTimeout);
       *abort_flag = 1;
-      // let the copies already issued land before the CTA exits
-      for (int i = 0; i < a.stages; ++i)
-        if (issued_phase[i] >= 0) mbar_wait(&full[i], (uint32_t)issued_phase[i], nullptr);
     }
+    // let the copies already issued land before the CTA exits: after an
+    // abort the issuer may not have read them all (on the normal path it
+    // has, and these waits end at once)
+    for (int i = 0; i < a.stages; ++i)
+      if (issued_phase[i] >= 0) mbar_wait(&full[i], (uint32_t)issued_phase[i], nullptr);
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer ----------------
     const uint32_t idesc = umma_idesc_bf16_f32(kVT, a.nc);

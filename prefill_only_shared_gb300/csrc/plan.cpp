@@ -492,7 +492,7 @@ sp_status build(const sp_shape* shape, sp_cache* cache, int32_t n_branches,
       call.n_append = (int64_t)appends.size() - call.append_off;
       // When the call has fewer tiles than one wave of CTAs, split the long
       // tiles' KV walks into parts (merged afterwards) so the call fills the
-      // GPU, keeping the total within one wave; then schedule longest first.
+      // GPU, keeping the total within one wave; then order them (below).
       const bool split_mode = (int64_t)raw.size() < part_target;
       // Otherwise pair the last tiles of sibling leaves whose tokens fit one
       // 128-row half each: one CTA walks their common ancestors once, then
@@ -559,8 +559,17 @@ sp_status build(const sp_shape* shape, sp_cache* cache, int32_t n_branches,
         }
         parts += np;
       }
-      std::stable_sort(work.begin(), work.end(),
-                       [](const Work& a, const Work& b) { return a.units > b.units; });
+      // Blocks start in list order.  Requests go one after another, so the
+      // CTAs running at any moment read the KV of one or two requests, which
+      // stays in L2 (taking every request's longest tiles first instead mixes
+      // all of a batch's requests at once: a 64-request batch then read its
+      // K / V from DRAM about four times over).  Within a request the longest
+      // tiles go first, so the last blocks of the call are short ones.
+      std::stable_sort(work.begin(), work.end(), [&](const Work& a, const Work& b) {
+        const int32_t ra = P->seg_req[a.t.seg], rb = P->seg_req[b.t.seg];
+        if (ra != rb) return ra < rb;
+        return a.units > b.units;
+      });
       call.tile_off = (int64_t)tiles.size();
       for (auto& w : work) tiles.push_back(w.t);
       call.n_tiles = (int64_t)work.size();

@@ -15,8 +15,20 @@ The model follows the kernel's order of waits, arrivals and commits,
 including the halves' turns on the tensor pipe (A0 B0 A1 B1 ...: p_full of
 one half also counts the other half's issue); each barrier counts its
 completions, and a wait names the completion it needs (the parity the kernel
-passes is that index's low bit).  Planted slips (a missing wait, a wrong
-arrival count) are caught; see the last test."""
+passes is that index's low bit).
+
+The abort paths are modelled too: any wait may give up (its time limit ran
+out), which raises the CTA's abort flag; every other role's wait then returns
+false unless its phase is already complete.  Each role then follows the
+kernel's abort sequence: a producer waits for the loads it issued (it always
+does, before the exit), an issuer commits and waits for all of its products
+on a drain barrier of its own (o_full completes only when all of a half's
+products ran, so the softmax never reads a partial O), the softmax stops.
+Every role must still end, with no product or load in flight when the CTA
+releases TMEM and exits, and TMEM released once.
+
+Planted slips (a missing wait, a wrong arrival count, an abort path that
+leaves work in flight) are caught; see the last tests."""
 import random
 
 import pytest
@@ -37,8 +49,10 @@ class Barrier:
 
 
 class Model:
-    def __init__(self, n_units, n_halves, seed, slip=None):
+    def __init__(self, n_units, n_halves, seed, slip=None, timeout_p=0.0):
         self.n, self.H, self.rng, self.slip = n_units, n_halves, random.Random(seed), slip
+        self.timeout_p, self.timed_out, self.abort = timeout_p, False, False
+        self.tmem_frees = 0
         B = Barrier
         paired = n_halves == 2
         self.q_full = B("q_full", 1)
@@ -50,6 +64,7 @@ class Model:
         self.s_full = [B(f"s_full{h}", 1) for h in range(2)]
         self.p_full = [B(f"p_full{h}", 4 + (1 if paired else 0)) for h in range(2)]
         self.o_full = [B(f"o_full{h}", 1) for h in range(2)]
+        self.drain = [B(f"drain{h}", 1) for h in range(2)]
         self.first_turn = B("first_turn", 1)
         # data: what each buffer holds (None: being loaded)
         self.k_stage = [None] * K_STAGES
@@ -75,28 +90,46 @@ class Model:
         stage = self.k_stage if is_k else self.v_stage
         if is_k:
             self.tma.append((None, None, None, self.q_full))
+        issued = [None] * n_st
+        ok = True
         for it in range(self.n):
             s = it % n_st
-            yield empty[s], it // n_st - 1  # the stage's previous use is done
+            if it >= n_st:  # the stage's previous use is done
+                ok = yield ("wait", empty[s], it // n_st - 1, True)
+                if not ok:
+                    break
             stage[s] = None
             self.tma.append((stage, s, it, full[s]))
+            issued[s] = it // n_st
+        if not ok:
+            self.abort = True
+        # every load issued has landed before the CTA exits
+        if self.slip != "producer_leaves_loads":
+            if is_k:
+                yield ("wait", self.q_full, 0, False)
+            for s in range(n_st):
+                if issued[s] is not None:
+                    yield ("wait", full[s], issued[s], False)
 
     def issuer(self, h):
         """Group g = PV_h(g-1) (g > 0) then QK_h(g) (g < n); the data waits,
         then the turn, then the issues; with two halves an arrival hands the
         turn to the other half."""
         paired = self.H == 2
-        yield self.q_full, 0
-        for g in range(self.n + 1):
+        ok = yield ("wait", self.q_full, 0, True)
+        g = 0
+        while ok and g <= self.n:
             do_pv, do_qk = g > 0, g < self.n
             if do_qk:
-                yield self.k_full[g % K_STAGES], g // K_STAGES
-            if do_pv:
-                yield self.v_full[(g - 1) % V_STAGES], (g - 1) // V_STAGES
-                if self.slip != "no_p_full_wait":
-                    yield self.p_full[h], g - 1
-            if paired and h == 1 and g == 0:
-                yield self.first_turn, 0
+                ok = yield ("wait", self.k_full[g % K_STAGES], g // K_STAGES, True)
+            if ok and do_pv:
+                ok = yield ("wait", self.v_full[(g - 1) % V_STAGES], (g - 1) // V_STAGES, True)
+                if ok and self.slip != "no_p_full_wait":
+                    ok = yield ("wait", self.p_full[h], g - 1, True)
+            if ok and paired and h == 1 and g == 0:
+                ok = yield ("wait", self.first_turn, 0, True)
+            if not ok:
+                break
             if do_pv:
                 self.pv_in_flight[h] += 1
                 self.pipe.append(("pv", h, g - 1, (g - 1) % V_STAGES))
@@ -109,19 +142,38 @@ class Model:
             if do_qk:
                 self.pipe.append(("commit", self.s_full[h]))
                 self.pipe.append(("commit", self.k_empty[g % K_STAGES]))
-        self.pipe.append(("commit", self.o_full[h]))
+            g += 1
+        if ok:
+            self.pipe.append(("commit", self.o_full[h]))
+            yield ("wait", self.o_full[h], 0, False)
+        else:
+            # gave up: o_full stays incomplete; the products issued so far
+            # drain before the exit
+            self.abort = True
+            if self.slip == "o_full_on_abort":  # the softmax could read a partial O
+                self.pipe.append(("commit", self.o_full[h]))
+                yield ("wait", self.o_full[h], 0, False)
+            elif self.slip != "issuer_leaves_products":
+                self.pipe.append(("commit", self.drain[h]))
+                yield ("wait", self.drain[h], 0, False)
 
     def softmax_warp(self, h, w):
         for it in range(self.n):
-            yield self.s_full[h], it
+            ok = yield ("wait", self.s_full[h], it, True)
+            if not ok:
+                self.abort = True
+                return
             assert self.S[h][w] == ("S", it), ("softmax reads S", h, w, it, self.S[h][w])
             if it > 0:
                 # the commit after QK_h(it) covers P.V of unit it-1: O_h is stable
                 assert self.pv_in_flight[h] == 0 and self.o_units[h] == it
             self.S[h][w] = ("P", it)  # this warp's rows of P_h, over S_h
             self.p_full[h].arrive()
-        yield self.o_full[h], 0
-        assert self.o_units[h] == self.n
+        ok = yield ("wait", self.o_full[h], 0, True)
+        if not ok:
+            self.abort = True
+            return
+        assert self.o_units[h] == self.n, ("epilogue reads a partial O", h)
 
     def step_pipe(self):
         op = self.pipe.pop(0)
@@ -154,18 +206,28 @@ class Model:
         waiting = [None] * len(roles)
         live = set(range(len(roles)))
 
-        def advance(i):
+        def advance(i, value=None):
             try:
-                waiting[i] = next(roles[i])
+                waiting[i] = roles[i].send(value) if value is not None else next(roles[i])
             except StopIteration:
                 live.discard(i)
                 waiting[i] = None
 
         for i in range(len(roles)):
             advance(i)
-        while True:
-            runnable = [i for i in live if waiting[i] is None or self.ready(*waiting[i])]
-            choices = [("role", i) for i in runnable]
+        while live:
+            choices = []
+            for i in live:
+                _, bar, k, abortable = waiting[i]
+                if self.ready(bar, k):
+                    choices.append(("go", i))
+                elif abortable and self.abort:
+                    choices.append(("stop", i))  # the wait saw the abort flag
+                elif (abortable and self.timeout_p and not self.timed_out
+                      and self.rng.random() < self.timeout_p):
+                    # its time limit ran out (the abort sequences' own waits
+                    # are bounded too, but their engines always finish)
+                    choices.append(("timeout", i))
             if self.pipe:
                 choices.append(("pipe", None))
             if self.tma:
@@ -173,22 +235,34 @@ class Model:
             if not choices:
                 break
             kind, i = self.rng.choice(choices)
-            if kind == "role":
-                advance(i)
+            if kind == "go":
+                advance(i, True)
+            elif kind == "stop":
+                advance(i, False)
+            elif kind == "timeout":
+                self.timed_out = True
+                advance(i, False)
             elif kind == "pipe":
                 self.step_pipe()
             else:
                 self.step_tma()
         assert not live, "deadlock: " + str(
-            [(waiting[i][0].name, waiting[i][1]) for i in sorted(live)])
-        assert not self.pipe and not self.tma
+            [(waiting[i][1].name, waiting[i][2]) for i in sorted(live)])
+        # every role reached the final block barrier: TMEM is released (once)
+        # and the CTA exits; nothing may still be in flight
+        assert not self.pipe, "products or commits in flight at exit"
+        assert not self.tma, "loads in flight at exit"
+        self.tmem_frees += 1
+        assert self.tmem_frees == 1
+        return self
 
 
 @pytest.mark.parametrize("n_halves", [1, 2])
 @pytest.mark.parametrize("n_units", [1, 2, 3, 4, 7, 16])
 def test_protocol_random_interleavings(n_units, n_halves):
     for seed in range(200):
-        Model(n_units, n_halves, seed).run()
+        m = Model(n_units, n_halves, seed).run()
+        assert not m.abort and m.o_units[:n_halves] == [n_units] * n_halves
 
 
 @pytest.mark.parametrize("slip", ["no_p_full_wait", "v_empty_one_half"])
@@ -198,6 +272,31 @@ def test_planted_slips_are_caught(slip):
         for seed in range(100):
             try:
                 Model(n_units, 2, seed, slip).run()
+            except AssertionError:
+                caught += 1
+    assert caught > 0
+
+
+@pytest.mark.parametrize("n_halves", [1, 2])
+@pytest.mark.parametrize("n_units", [1, 2, 5, 9])
+def test_any_wait_may_give_up(n_units, n_halves):
+    """One wait, anywhere, runs out of time: the abort flag stops the others,
+    every role ends and nothing is left in flight."""
+    aborted = 0
+    for seed in range(300):
+        m = Model(n_units, n_halves, seed, timeout_p=0.02).run()
+        aborted += m.abort
+    assert aborted > 50
+
+
+@pytest.mark.parametrize("slip", ["producer_leaves_loads", "issuer_leaves_products",
+                                  "o_full_on_abort"])
+def test_abort_slips_are_caught(slip):
+    caught = 0
+    for n_units in (2, 3, 5):
+        for seed in range(200):
+            try:
+                Model(n_units, 2, seed, slip, timeout_p=0.05).run()
             except AssertionError:
                 caught += 1
     assert caught > 0

@@ -257,11 +257,12 @@ def test_descriptor_tiny_config(lib):
 
 
 @pytest.mark.parametrize("n_sms", [1, 8, 152])
-@pytest.mark.parametrize("name", ["tiny", "yesno", "choice64", "tree2"])
+@pytest.mark.parametrize("name", ["tiny", "yesno", "choice64", "tree2", "batch64"])
 def test_tiles_are_listed_longest_first(lib, name, n_sms):
     """Blocks start in list order, so every call lists its tiles (and split
-    parts) by non-increasing KV units; paired tiles appear only in calls that
-    are not split."""
+    parts) request by request, in increasing request id (the KV a moment's
+    CTAs read stays in L2), and within a request by non-increasing KV units;
+    paired tiles appear only in calls that are not split."""
     wl = make_workload(name, tokens_only=True)
     sh = wl.shape
     plan = lib.sp_plan_build(lib.make_shape(sh.n_q_heads, sh.n_kv_heads, sh.head_dim, 16,
@@ -274,6 +275,9 @@ def test_tiles_are_listed_longest_first(lib, name, n_sms):
             ci = plan.call_info(rnd, kind)
             t = tiles[ci["tile_off"]:ci["tile_off"] + ci["n_tiles"]]
             units = (t["u_hi"] - t["u_lo"]).astype(np.int64)
-            assert (np.diff(units) <= 0).all(), (rnd, kind)
+            req = plan.segments()["req"][t["seg"]]
+            assert (np.diff(req) >= 0).all(), (rnd, kind)
+            for r in np.unique(req):
+                assert (np.diff(units[req == r]) <= 0).all(), (rnd, kind, r)
             if ci["n_parts"] > 0:
                 assert (t["seg2"] < 0).all(), (rnd, kind)
