@@ -565,11 +565,17 @@ typedef struct sp_input_set {
  *      set has finished, so its buffers and staging can be overwritten;
  *   3. on copy_stream: copies q_host, k_host, v_host (node_rows rows each),
  *      h_host (n_branches rows), label_off_host (n_branches + 1) and
- *      label_ids_host (n_labels) into the set, then records copied_event;
- *   4. on stream: waits for copied_event, uploads the descriptor from
- *      desc_host, runs the tree attention, readout and softmax on the set's
- *      buffers, copies probs and argmax to probs_host and argmax_host, and
- *      records done_event.
+ *      label_ids_host (n_labels) into the set, then uploads the descriptor
+ *      from desc_host into desc (after any earlier sp_run_pass_host pass
+ *      that reads the same desc buffer has finished: the library keeps one
+ *      event per recently used desc buffer for this), then records
+ *      copied_event;
+ *   4. on stream: waits for copied_event, runs the tree attention, readout
+ *      and softmax on the set's buffers, copies probs and argmax to
+ *      probs_host and argmax_host, and records done_event.
+ * The descriptor travels on copy_stream so that it reaches the copy engine
+ * before the next call's input copies; on stream it would wait behind them
+ * and the pass could not overlap the next call's copies.
  * Once step 3 has been enqueued, done_event is recorded even when a later
  * step fails.  The outputs in host memory are ready once done_event has
  * completed (or `stream` is synchronised).  All host buffers but tokens and

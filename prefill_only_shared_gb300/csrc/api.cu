@@ -462,6 +462,49 @@ extern "C" sp_status sp_run_pass(const sp_shape* shape, int32_t n_branches,
   return st;
 }
 
+// One library-owned event per (device, descriptor buffer) that
+// sp_run_pass_host has uploaded into: recorded after each pass that reads the
+// buffer, waited for by the copy stream before the next upload into it.
+// Events are created on first use (no device memory); the table keeps the
+// most recent buffers and hands out a slot of the least recently used one
+// when full (its event was recorded passes ago, so waiting on it costs
+// nothing).
+static cudaEvent_t desc_release_event(const void* desc) {
+  struct Slot {
+    const void* desc;
+    int device;
+    cudaEvent_t ev;
+    uint64_t used;
+  };
+  constexpr int kSlots = 32;
+  static Slot slots[kSlots] = {};
+  static uint64_t clock = 0;
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  Slot* lru = &slots[0];
+  for (Slot& x : slots) {
+    if (x.ev && x.desc == desc && x.device == dev) {
+      x.used = ++clock;
+      return x.ev;
+    }
+    if (!x.ev || x.used < lru->used) lru = &x;
+  }
+  if (lru->ev && lru->device != dev) {
+    cudaEventDestroy(lru->ev);  // an event belongs to its device
+    lru->ev = nullptr;
+  }
+  if (!lru->ev && cudaEventCreateWithFlags(&lru->ev, cudaEventDisableTiming) != cudaSuccess) {
+    lru->ev = nullptr;
+    return nullptr;
+  }
+  lru->desc = desc;
+  lru->device = dev;
+  lru->used = ++clock;
+  return lru->ev;
+}
+
 extern "C" sp_status sp_run_pass_host(
     const sp_shape* shape, int32_t n_branches, const int32_t* req_of_branch,
     const int64_t* tok_offsets, const int32_t* tokens, int64_t node_rows, const void* q_host,
@@ -520,19 +563,29 @@ extern "C" sp_status sp_run_pass_host(
                            (size_t)n_labels * sizeof(int32_t)};
   for (int i = 0; i < 6 && ce == cudaSuccess; ++i)
     ce = cudaMemcpyAsync(dst[i], src[i], bytes[i], cudaMemcpyHostToDevice, cs);
+  // The descriptor goes up on the copy stream too, right behind this pass's
+  // inputs: on `stream` it would queue on the copy engine behind the next
+  // call's input copies (enqueued meanwhile on the copy stream), and the pass
+  // could not start before they end.  A pass that still reads the same
+  // descriptor buffer (an earlier call's, when callers share one) finishes
+  // first.
+  cudaEvent_t desc_free = ce == cudaSuccess ? desc_release_event(desc) : nullptr;
+  if (ce == cudaSuccess && !desc_free) ce = cudaErrorUnknown;
+  if (ce == cudaSuccess) ce = cudaStreamWaitEvent(cs, desc_free, 0);
+  if (ce == cudaSuccess)
+    ce = cudaMemcpyAsync(desc, set->desc_host, blob, cudaMemcpyHostToDevice, cs);
   // however many copies were enqueued, they finish before anything `stream`
   // runs from here on, done_event included
   cudaError_t cw = cudaEventRecord(copied, cs);
   if (cw == cudaSuccess) cw = cudaStreamWaitEvent(ms, copied, 0);
   if (cw != cudaSuccess) cudaStreamSynchronize(cs);
   st = ce == cudaSuccess && cw == cudaSuccess ? SP_OK : SP_ERR_CUDA;
-  if (st == SP_OK &&
-      cudaMemcpyAsync(desc, set->desc_host, blob, cudaMemcpyHostToDevice, ms) != cudaSuccess)
-    st = SP_ERR_CUDA;
   if (st == SP_OK)
     st = launch_pass(plan, shape, n_branches, desc, set->q, set->k, set->v, kv_pool, out, lse,
                      attn_ws, attn_ws_bytes, set->h, W, set->label_off, set->label_ids, n_labels,
                      logprobs, lse_vocab, lm_ws, lm_ws_bytes, probs, argmax, stream);
+  // the next upload into this descriptor buffer waits for this pass
+  if (desc_free && cudaEventRecord(desc_free, ms) != cudaSuccess && st == SP_OK) st = SP_ERR_CUDA;
   sp_plan_free(plan);
   if (st == SP_OK &&
       (cudaMemcpyAsync(probs_host, probs, (size_t)n_labels * sizeof(float),
