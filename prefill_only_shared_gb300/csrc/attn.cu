@@ -707,8 +707,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      float sv[kKeysPerUnit];
-      tmem_ld128(trow + s_col, sv);
       // visible keys of this row in this unit: c < lim
       const int key0 = walk.cur.j * kKeysPerUnit;
       int lim = walk.cur.len - key0;
@@ -718,42 +716,60 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool other = td.seg2 >= 0 && ((walk.cur.level > sd.chain_len) != (h == 1));
         lim = other ? 0 : min(lim, token - key0 + 1);
       }
-      if (__any_sync(0xffffffffu, lim < kKeysPerUnit)) {
-#pragma unroll
-        for (int c = 0; c < kKeysPerUnit; ++c) sv[c] = c < lim ? sv[c] : -INFINITY;
-      }
-      // tree maximum: eight independent chains of three-input maxima
-      float mx8[8];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) mx8[c] = fmaxf(sv[2 * c], sv[2 * c + 1]);
-#pragma unroll
-      for (int c = 16; c < kKeysPerUnit; c += 2) mx8[(c >> 1) & 7] = max3(mx8[(c >> 1) & 7], sv[c], sv[c + 1]);
-      const float mt = fmaxf(max3(mx8[0], mx8[1], mx8[2]), fmaxf(max3(mx8[3], mx8[4], mx8[5]),
-                                                                 fmaxf(mx8[6], mx8[7])));
-      const float m_new = fmaxf(m_used, mt * scale);
-      float alpha = 1.f;
-      if (m_new > m_used + kRescaleLog2) {  // also true for the first finite max
-        alpha = m_used == -INFINITY ? 0.f : ex2(m_used - m_new);
-        m_used = m_new;
-      }
-      const float nbase = m_used == -INFINITY ? 0.f : -m_used;
-      const uint64_t sc2 = f2(scale, scale), nb2 = f2(nbase, nbase);
+      // The running maximum only keeps 2^(s * scale - m) finite: P, the row
+      // sum and O are exact in relative terms for any reference m, which
+      // cancels in O / l.  A row takes it on its first unit with a finite
+      // score, and again only when a unit's sum shows a score more than 64
+      // above the reference (P > 2^64) or a value that is not finite; that
+      // second pass reloads S (P goes over it only after the loop).
+      const float m_prev = m_used;
+      const bool masked = __any_sync(0xffffffffu, lim < kKeysPerUnit);
+      const uint64_t sc2 = f2(scale, scale);
       uint32_t pw[kKeysPerUnit / 2];
-      uint64_t sum4[4] = {0, 0, 0, 0};
+      float ls = 0.f;
+#pragma unroll 1
+      for (int pass = 0; pass < 2; ++pass) {
+        float sv[kKeysPerUnit];
+        tmem_ld128(trow + s_col, sv);
+        if (masked) {
 #pragma unroll
-      for (int c = 0; c < kKeysPerUnit; c += 2) {
-        float x0, x1;
-        uf2(fma_f2(f2(sv[c], sv[c + 1]), sc2, nb2), x0, x1);
-        const float p0 = ex2(x0), p1 = ex2(x1);
-        sum4[(c >> 1) & 3] = add_f2(sum4[(c >> 1) & 3], f2(p0, p1));
-        pw[c >> 1] = pack_bf16(p0, p1);
+          for (int c = 0; c < kKeysPerUnit; ++c) sv[c] = c < lim ? sv[c] : -INFINITY;
+        }
+        if (pass == 1 || __any_sync(0xffffffffu, m_used == -INFINITY)) {
+          // tree maximum: eight independent chains of three-input maxima
+          float mx8[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) mx8[c] = fmaxf(sv[2 * c], sv[2 * c + 1]);
+#pragma unroll
+          for (int c = 16; c < kKeysPerUnit; c += 2)
+            mx8[(c >> 1) & 7] = max3(mx8[(c >> 1) & 7], sv[c], sv[c + 1]);
+          const float mt = fmaxf(max3(mx8[0], mx8[1], mx8[2]),
+                                 fmaxf(max3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+          const float m_new = fmaxf(m_used, mt * scale);
+          // a first maximum, or an overflow; otherwise only a rise by > 2^8
+          if (pass == 1 || m_used == -INFINITY || m_new > m_used + kRescaleLog2) m_used = m_new;
+        }
+        const float nbase = m_used == -INFINITY ? 0.f : -m_used;
+        const uint64_t nb2 = f2(nbase, nbase);
+        uint64_t sum4[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int c = 0; c < kKeysPerUnit; c += 2) {
+          float x0, x1;
+          uf2(fma_f2(f2(sv[c], sv[c + 1]), sc2, nb2), x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          sum4[(c >> 1) & 3] = add_f2(sum4[(c >> 1) & 3], f2(p0, p1));
+          pw[c >> 1] = pack_bf16(p0, p1);
+        }
+        float s0, s1, s2, s3, s4, s5, s6, s7;
+        uf2(sum4[0], s0, s1);
+        uf2(sum4[1], s2, s3);
+        uf2(sum4[2], s4, s5);
+        uf2(sum4[3], s6, s7);
+        ls = ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
+        if (!__any_sync(0xffffffffu, !(ls <= 0x1p64f))) break;
       }
-      float s0, s1, s2, s3, s4, s5, s6, s7;
-      uf2(sum4[0], s0, s1);
-      uf2(sum4[1], s2, s3);
-      uf2(sum4[2], s4, s5);
-      uf2(sum4[3], s6, s7);
-      l = l * alpha + (((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7)));
+      const float alpha = m_used == m_prev ? 1.f : m_prev == -INFINITY ? 0.f : ex2(m_prev - m_used);
+      l = l * alpha + ls;
       // O_h is stable: PV_h of the previous unit completed before S_h arrived
       if (it > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
